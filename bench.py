@@ -1,0 +1,459 @@
+#!/usr/bin/env python
+"""Benchmark of one DDTree verify step on GB300; prints ONE JSON line.
+
+A step is the whole hot path through the C ABI (``ddt_step``): best-first
+tree build -> tree-verify MLA-absorb attention -> greedy accept + cache
+compaction, over one batch of the max-budget workload (B=1, D=16, K=8,
+budget 64 -> q_len 65, 64 heads, kv_lora 512, rope 64, prefix 4096, bf16).
+The step is captured in a CUDA graph and replayed; L2 is flushed (a 256 MiB
+write) between timed steps, outside the per-step CUDA events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c2]
+    python bench.py --impl reference ...     # the CPU oracle as the reference arm
+
+Multi-GPU (torchrun, one process per GPU) runs independent replicas: the
+path has no exchange step, so each rank verifies its own batch; ``value`` is
+all ranks' steps divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "DDTree verify steps/s; verify_attn TFLOP/s and % of GB300 roofline"
+FLUSH_BYTES = 256 << 20
+
+
+# --------------------------------------------------------------------- helpers
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="c2",
+                    help="c1..c4 or a sweep point q<len>_b<batch>_l<prefix>")
+    ap.add_argument("--no-graph", action="store_true", help="launch each step directly")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args(argv)
+
+
+def workload(name: str):
+    from tree_speculative_decoding_ddt_gb300 import workloads as WL
+    if name in WL.CONFIGS:
+        return WL.CONFIGS[name]
+    if name.startswith("q"):
+        q, b, l = name[1:].split("_")
+        return WL.sweep_point(int(q), int(b[1:]), int(l[1:]))
+    raise SystemExit(f"unknown config {name}")
+
+
+def describe(w) -> str:
+    pre = w.prefix if not isinstance(w.prefix, tuple) else f"U[{w.prefix[0]},{w.prefix[1]}]"
+    paging = f"paged {w.page_size}" if w.page_size else "contiguous"
+    return (f"{w.name}: B={w.B} D={w.D} K={w.K} V={w.V} budget={w.budget} (q_len {w.Q}) "
+            f"H={w.H} kv_lora={w.C} rope={w.R} prefix={pre} {paging} {w.dtype}")
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def attn_work(w, prefix_len, depths, dtype_bytes):
+    """Algorithmic FLOPs and bytes of one verify-attention launch: every
+    visible (query row, key) pair costs 2(C+R) for q.k and 2C for p.v; a
+    row sees its prefix plus its ancestor path (depth+1 tree slots). Bytes:
+    each cache row read once, Q read once, O written once, lse written."""
+    flops = 0
+    keys = 0
+    for b in range(w.B):
+        L = int(prefix_len[b])
+        d = np.asarray(depths[b])
+        n_vis = L + np.where(d >= 0, d + 1, 1)
+        flops += int(n_vis.sum()) * w.H * (4 * w.C + 2 * w.R)
+        keys += L + w.Q
+    byt = (keys * (w.C + w.R) * dtype_bytes + w.B * w.Q * w.H * (w.C + w.R) * dtype_bytes
+           + w.B * w.Q * w.H * w.C * dtype_bytes + w.B * w.Q * w.H * 4)
+    return flops, byt
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [r for r in rows if r[2] > 0.25 * max(x[2] for x in rows)] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3][1:5])
+                          if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(loaded), "power_w_max": max(r[2] for r in rows)}
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest value of ``x`` over all ranks (identity without a process group)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------- CPU oracle arm
+
+def oracle_steps(w, batch, seconds: float, max_steps: int):
+    """Time whole oracle steps (heapq build, float64 attention, accept,
+    compaction) until about ``seconds`` have passed; returns (steps, secs)."""
+    from oracle import ddt_oracle as O
+    from tree_speculative_decoding_ddt_gb300 import workloads as WL
+    lay = batch.layout
+    n = 0
+    t0 = time.perf_counter()
+    while n < max_steps:
+        O.ddt_step(batch.topk_logp, batch.topk_ids, batch.root_tok, w.budget, w.V, batch.q_lat,
+                   batch.q_pe, batch.kv, lay.block_table, batch.prefix_len, w.scale,
+                   lay.page_size, lay.max_pages,
+                   lambda t: WL.target_argmax_for(batch, t["depths"]))
+        n += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    return n, time.perf_counter() - t0
+
+
+def cpu_info():
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    model = ""
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                model = line.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    import platform
+    return cores, f"{platform.machine()} {model}".strip()
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from tree_speculative_decoding_ddt_gb300 import workloads as WL
+    w = workload(args.config)
+    batch = WL.make_batch(w)
+    if args.warmup > 0:
+        oracle_steps(w, batch, 0.0, 1)
+    n, secs = oracle_steps(w, batch, args.cpu_seconds, max(1, args.steps))
+    cores, model = cpu_info()
+    v = n / secs
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": args.gpus,
+        "steps": n, "warmup": min(args.warmup, 1), "ms_per_step": 1e3 * secs / n,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": describe(w)},
+        "cpu_baseline": {"value": v, "unit": "steps/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} whole oracle steps (python heapq build, numpy float64 "
+                                   f"attention, accept, compaction) on {model}"},
+        "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_ours(args):
+    import torch
+    from tree_speculative_decoding_ddt_gb300 import _binding as DB
+    from tree_speculative_decoding_ddt_gb300 import workloads as WL
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    DB.load()
+
+    w = workload(args.config)
+    batch = WL.make_batch(w)
+    lay = batch.layout
+    bf16 = w.dtype == "bf16"
+    dt = DB.DDT_BF16 if bf16 else DB.DDT_F32
+    max_len = int(batch.prefix_len.max()) + w.Q
+    buf = DB.StepBuffers(w.B, w.D, w.K, w.budget, w.V, w.H, w.C, w.R, lay.page_size,
+                         lay.max_pages, lay.total_rows, dt, w.scale, max_len, device=dev)
+
+    def dev_lat(x):
+        if bf16:
+            bits = WL.to_bf16_bits(x).view(np.int16)
+            return torch.from_numpy(np.ascontiguousarray(bits)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(dev)
+
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
+    buf.topk_logp.copy_(torch.from_numpy(batch.topk_logp).to(dev))
+    buf.topk_ids.copy_(i32(batch.topk_ids))
+    buf.root_tok.copy_(i32(batch.root_tok))
+    buf.q_lat.copy_(dev_lat(batch.q_lat))
+    buf.q_pe.copy_(dev_lat(batch.q_pe))
+    buf.kv_cache.copy_(dev_lat(batch.kv))
+    buf.block_table.copy_(i32(lay.block_table))
+    buf.prefix_len.copy_(i32(batch.prefix_len))
+    # the synthetic target's argmax depends on each slot's depth: build the
+    # (deterministic) tree once to read the depths
+    tr = DB.ddt_tree_build(buf.topk_logp, buf.topk_ids, buf.root_tok, w.budget, w.V)
+    depths = tr["depths"].cpu().numpy()
+    buf.target_argmax.copy_(i32(WL.target_argmax_for(batch, depths)))
+    torch.cuda.synchronize()
+
+    split = DB.ddt_verify_attn_workspace_size(buf.attn) > 0
+    launches_per_step = 3 + (1 if split else 0)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        DB.ddt_step(buf)
+
+    def attn_only():
+        DB.ddt_verify_attn(buf.q_lat, buf.q_pe, buf.kv_cache, buf.block_table, buf.prefix_len,
+                           buf.vis_bits, w.scale, lay.page_size, max_len, out=buf.out,
+                           lse=buf.lse, status=buf.status, workspace=buf.workspace)
+
+    use_graph = not args.no_graph
+    graphs = {}
+    if use_graph:
+        for name, fn in (("step", step), ("attn", attn_only)):
+            fn()  # warm the kernels up once before capture
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+            graphs[name] = g
+    run = {k: (graphs[k].replay if use_graph else f) for k, f in
+           (("step", step), ("attn", attn_only))}
+
+    def timed(fn, n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for s, e in evs:
+            flush.fill_(1)
+            s.record(stream)
+            fn()
+            e.record(stream)
+        return evs
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1)
+        run["step"]()
+    torch.cuda.synchronize()
+
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        evs = timed(run["step"], args.steps)
+        torch.cuda.synchronize()
+        barrier(world)
+        bracket_s = time.perf_counter() - t0
+        step_ms = [s.elapsed_time(e) for s, e in evs]
+        # the dominant kernel, timed the same way
+        n_attn = max(50, args.steps // 4)
+        aevs = timed(run["attn"], n_attn)
+        torch.cuda.synchronize()
+        attn_ms = [s.elapsed_time(e) for s, e in aevs]
+    clocks = clk.summary()
+
+    # end to end through the public API: host inputs in pinned memory are
+    # copied in, the step runs, its result (accepted tokens, lengths, status)
+    # is copied out, every step
+    host_in = {
+        "topk_logp": torch.from_numpy(batch.topk_logp).pin_memory(),
+        "topk_ids": torch.from_numpy(batch.topk_ids).pin_memory(),
+        "root_tok": torch.from_numpy(batch.root_tok).pin_memory(),
+        "q_lat": torch.from_numpy(np.ascontiguousarray(WL.to_bf16_bits(batch.q_lat).view(np.int16)
+                                                       if bf16 else batch.q_lat)).pin_memory(),
+        "q_pe": torch.from_numpy(np.ascontiguousarray(WL.to_bf16_bits(batch.q_pe).view(np.int16)
+                                                      if bf16 else batch.q_pe)).pin_memory(),
+        "target_argmax": torch.from_numpy(WL.target_argmax_for(batch, depths)).pin_memory(),
+    }
+    tree_rows = np.concatenate([lay.rows_of(b, np.arange(int(batch.prefix_len[b]),
+                                                         int(batch.prefix_len[b]) + w.Q))
+                                for b in range(w.B)])
+    tree_lat = batch.kv[tree_rows]
+    host_tree = torch.from_numpy(np.ascontiguousarray(
+        WL.to_bf16_bits(tree_lat).view(np.int16) if bf16 else tree_lat)).pin_memory()
+    tree_rows_dev = torch.from_numpy(tree_rows).to(dev)
+    tree_dev = torch.empty_like(host_tree, device=dev)
+    outs = [buf.out_tokens, buf.accept_len, buf.new_len, buf.status]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + \
+        host_tree.numel() * host_tree.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    kv_view = buf.kv_cache.view(torch.int16) if bf16 else buf.kv_cache
+
+    def e2e_step():
+        for k, h in host_in.items():
+            dst = getattr(buf, k)
+            (dst.view(torch.int16) if dst.dtype == torch.bfloat16 else dst).copy_(h, non_blocking=True)
+        tree_dev.copy_(host_tree, non_blocking=True)
+        kv_view.index_copy_(0, tree_rows_dev, tree_dev)  # cache append of the tree latents
+        DB.ddt_step(buf)
+        for h, t in zip(host_out, outs):
+            h.copy_(t, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    n_e2e = max(20, min(args.steps, 2000))
+    for _ in range(3):
+        e2e_step()
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        e2e_step()
+    e2e_s = time.perf_counter() - t0
+
+    st = buf.status.cpu().numpy()
+    if (st & ~DB.ST_BUDGET_PAD).any():
+        raise SystemExit(f"device status reports errors: {st}")
+
+    sum_s = sum(step_ms) / 1e3
+    slowest = max_over_ranks(sum_s, world, dev)
+    value = world * args.steps / slowest
+    flops, byt = attn_work(w, batch.prefix_len, depths, 2 if bf16 else 4)
+    attn_s = statistics.mean(attn_ms) / 1e3
+    hbm, tf, src = measured_peaks()
+    achieved_tf = flops / attn_s / 1e12
+    achieved_gb = byt / attn_s / 1e9
+    t_roof = max(flops / (tf * 1e12), byt / (hbm * 1e9))
+    bound = "tensor" if flops / (tf * 1e12) >= byt / (hbm * 1e9) else "hbm"
+    line = {
+        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup),
+        "ms_per_step": 1e3 * slowest / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded numpy generators)",
+        "config": {"workload": describe(w), "parallelism": f"replicas x{world}",
+                   "l2": "flushed by a 256 MiB write before every timed step, outside its events",
+                   "launch": "cuda_graph replay" if use_graph else "direct C-ABI calls",
+                   "bracket_s_incl_flush": bracket_s},
+        "roofline": {
+            "kernel": "ddt_verify_attn (tcgen05 attention + split merge)" if bf16
+                      else "ddt_verify_attn (fp32 SIMT)",
+            "bound": bound if bf16 else "alu",
+            "achieved": achieved_tf if bound == "tensor" else achieved_gb,
+            "peak": tf if bound == "tensor" else hbm,
+            "unit": "TFLOP/s" if bound == "tensor" else "GB/s",
+            "frac": (achieved_tf / tf) if bound == "tensor" else (achieved_gb / hbm),
+            "peak_source": f"{src} (MEASURED_PEAKS.json burst)" if src == "measured" else src,
+            "traffic": None,
+            "algorithmic_flops": flops, "algorithmic_bytes": byt,
+            "attn_us": attn_s * 1e6, "roofline_us": t_roof * 1e6,
+            "frac_of_roofline_time": t_roof / attn_s,
+        },
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "e2e": {"value": world * n_e2e / max_over_ranks(e2e_s, world, dev), "unit": "steps/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms)},
+    }
+    if rank == 0 and world == 1:
+        n_cpu = max(1, int(args.cpu_seconds // 2))
+        n, secs = oracle_steps(w, batch, args.cpu_seconds, n_cpu * 50)
+        cores, model = cpu_info()
+        line["cpu_baseline"] = {
+            "value": n / secs, "unit": "steps/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} whole oracle steps of the same workload (python heapq build, numpy "
+                      f"float64 attention, accept, compaction) on {model}"}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

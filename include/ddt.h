@@ -1,0 +1,265 @@
+/*
+ * ddt.h -- C ABI of the GB300 (sm_103a) DDTree verify step.
+ *
+ * One verify step of draft-tree speculative decoding, as a native engine runs
+ * it ("The Checkpoint: Committing a Working Native DDTree Engine", section
+ * "The Message": generate_ddtree wires tree_build -> verify_attn ->
+ * tree_accept + cache compaction):
+ *
+ *   A. ddt_tree_build     best-first draft tree from the drafter's per-depth
+ *                         top-k log-probs
+ *   B. ddt_verify_attn    tree-verify MLA-absorb attention over the latent
+ *                         cache, mask [ones over prefix | tree visibility]
+ *   C. ddt_tree_accept    greedy walk from the root, bonus token
+ *   D. ddt_cache_compact  gather of the accepted-path latents
+ *   ddt_step              A -> B -> C+D on one stream
+ *
+ * Conventions (all entry points):
+ *  - Every pointer argument is DEVICE memory owned by the caller, except the
+ *    dims/args structs, which are read on the host during the call. The
+ *    library keeps no pointer after it returns and allocates no device memory;
+ *    scratch space is passed in (size it with the *_workspace_size query).
+ *  - Work is enqueued on `stream` and the call returns without synchronising.
+ *    Results are ready when the stream reaches them.
+ *  - The return value reports problems found on the HOST (bad sizes, null
+ *    pointers, unsupported dimensions, launch failures): DDT_OK or a negative
+ *    DDT_E* code; nothing was enqueued when it is negative (DDT_ELAUNCH: some
+ *    earlier kernels of the same call may have been enqueued).
+ *  - Problems in the DATA are found on the device and reported per sequence
+ *    in `status` (int32[B]) as DDT_ST_* bits; kernels never trap and every
+ *    device loop is bounded. ddt_tree_build and ddt_step overwrite status[b];
+ *    ddt_verify_attn, ddt_tree_accept and ddt_cache_compact OR their bits in.
+ *  - Integer arrays are int32, row-major, densely packed (strides in the
+ *    comments). Nodes of a tree are numbered in the order the builder pops
+ *    them: slot 0 is the root, and every node's parent has a lower slot.
+ *  - Thread-compatible: calls on different streams may run concurrently; the
+ *    library's only global state is a per-device cache of device properties.
+ */
+#ifndef DDT_H_
+#define DDT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- host return codes ---------------------------------------------------- */
+#define DDT_OK 0
+#define DDT_EINVAL (-1)       /* invalid argument (null pointer, negative size, ...) */
+#define DDT_EUNSUPPORTED (-2) /* valid but outside what this build supports */
+#define DDT_ELAUNCH (-3)      /* a CUDA launch or query failed */
+#define DDT_EWORKSPACE (-4)   /* workspace missing or smaller than required */
+
+/* ---- per-sequence device status bits ------------------------------------- */
+#define DDT_ST_BUDGET_PAD 1  /* tree has fewer than budget+1 nodes; the rest is padding (informational) */
+#define DDT_ST_INPUT 2       /* non-finite log-prob, or a token id outside [0, V) */
+#define DDT_ST_CYCLE 4       /* accept walk would revisit a node (malformed tree) */
+#define DDT_ST_RANGE 8       /* accept path / slot outside the cache; sequence left untouched */
+#define DDT_ST_CAPACITY 16   /* prefix_len + q_len exceeds the sequence's cache capacity */
+#define DDT_ST_TIMEOUT 32    /* a device-side wait ran past its bound; this sequence's outputs are not valid */
+
+/* ---- element types -------------------------------------------------------- */
+#define DDT_F32 0  /* float32 inputs and outputs; SIMT fp32 arithmetic (exactness path) */
+#define DDT_BF16 1 /* bfloat16 inputs and outputs; tensor cores, fp32 accumulation */
+
+/* Largest supported q_len (= budget + 1); the mask of a query row is
+ * W = ceil(q_len / 64) uint64 words. */
+#define DDT_MAX_Q 128
+
+/* Shapes of the tree build. B sequences, D draft depths, K candidates per
+ * depth, budget draft nodes (q_len = budget + 1 tree slots), vocabulary V. */
+typedef struct ddt_tree_dims {
+  int32_t B, D, K, budget, V;
+} ddt_tree_dims;
+
+/* Shapes of the verify attention.
+ *  B sequences, Q = q_len tree queries per sequence, H query heads,
+ *  C = kv_lora_rank (latent width), R = rope width; the cache row of a token
+ *  is [c_kv (C) | k_pe (R)].
+ *  The cache is paged: slot s of sequence b lives in physical row
+ *  block_table[b * max_pages + s / page_size] * page_size + s % page_size of a
+ *  [kv_rows, C+R] array (a contiguous cache is max_pages = 1 with a page per
+ *  sequence). scale multiplies q.k. max_len is a host-side upper bound of
+ *  prefix_len[b] + Q over the batch; it only sizes the split of the key range
+ *  (and so the workspace), results are correct for any length that fits the
+ *  cache. */
+typedef struct ddt_attn_dims {
+  int32_t B, Q, H, C, R;
+  int32_t page_size, max_pages;
+  int32_t dtype; /* DDT_F32 or DDT_BF16 */
+  int64_t kv_rows;
+  float scale;
+  int32_t max_len;
+} ddt_attn_dims;
+
+/* A. Best-first draft-tree construction.
+ * "The Milestone Commit: Cementing a Native DDTree Inference Engine", sections
+ * "What the Message Actually Does" (GPU best-first tree builder, double
+ * accumulation for parity, ancestor-bitmask visibility, first-child /
+ * next-sibling retrieve) and "The Reasoning Behind the Architecture".
+ *
+ * Node score = sum of the log-probs along its path, accumulated in double
+ * (child = parent + (double)logp). Starting from the root (score 0), the best
+ * frontier node is popped, then its first child (rank 0, one depth down) and
+ * its next sibling (rank+1, same parent) are pushed; order is score
+ * descending, then depth ascending, then rank ascending, then parent slot
+ * ascending. Construction stops after `budget` pops. Every node at depth d
+ * takes its token and log-prob from row d-1 of the drafter's top-k.
+ *
+ * In:  topk_logp f32[B][D][K] (rank 0 first), topk_ids i32[B][D][K],
+ *      root_tok i32[B] (the verified token at slot 0).
+ * Out (Q = budget+1, W = ceil(Q/64)):
+ *      tokens, parents (root -1), depths (root 0): i32[B][Q];
+ *      vis_bits u64[B][Q][W]: bit t of word t/64 of row n is set iff slot t is
+ *        n or an ancestor of n;
+ *      vis u8[B][Q][Q] (may be NULL): the same mask expanded, 1 = visible;
+ *      first_child, next_sibling i32[B][Q] (-1 = none; lowest slot first);
+ *      n_nodes i32[B]; status i32[B] (overwritten).
+ * Slots n_nodes..Q-1 (only when the candidate tree is smaller than the budget,
+ * DDT_ST_BUDGET_PAD) hold token 0, parent -1, depth -1, self-visibility only.
+ * A NaN/inf log-prob or an id outside [0, V) sets DDT_ST_INPUT and yields the
+ * root alone. Limits: 1 <= B, 1 <= D, 1 <= K, 0 <= budget < DDT_MAX_Q,
+ * min(D,budget) * min(K,budget) <= 8192, V >= 1. */
+int ddt_tree_build(const ddt_tree_dims* dims, const float* topk_logp, const int32_t* topk_ids,
+                   const int32_t* root_tok, int32_t* tokens, int32_t* parents, int32_t* depths,
+                   uint64_t* vis_bits, uint8_t* vis, int32_t* first_child, int32_t* next_sibling,
+                   int32_t* n_nodes, int32_t* status, cudaStream_t stream);
+
+/* Bytes of scratch ddt_verify_attn needs for these dims (0 = none). */
+size_t ddt_verify_attn_workspace_size(const ddt_attn_dims* dims);
+
+/* B. Tree-verify MLA-absorb attention.
+ * "The Checkpoint: Committing a Working Native DDTree Engine", section "The
+ * Message" (attention via the custom verify_attn in absorb form; KV-cache
+ * scheme: the tree [verified_id, drafts] sits at cache positions L+depth,
+ * prefix = cache length, mask = [ones | visibility], AR = degenerate
+ * q_len = 1) and "The Milestone Commit", section "Input Knowledge Required"
+ * (MLA latent cache, kv_lora_rank 512 for Kimi K2.6).
+ *
+ * For sequence b (L = prefix_len[b]), tree query i and head h:
+ *   s_j = (q_lat[b,i,h,:] . c_kv[j,:] + q_pe[b,i,h,:] . k_pe[j,:]) * scale
+ * over key slots j in [0, L) (always visible) and j = L + t for tree slots t
+ * visible from i (bit t of vis_bits[b][i]); p = softmax(s);
+ *   out[b,i,h,:] = sum_j p_j c_kv[j,:],  lse[b,i,h] = log sum_j exp(s_j).
+ * The caller has already written the tree nodes' latents into slots
+ * [L, L+Q) in node (slot) order.
+ *
+ * q_lat [B][Q][H][C], q_pe [B][Q][H][R], kv_cache [kv_rows][C+R], out
+ * [B][Q][H][C]: element type dims->dtype. block_table i32[B][max_pages],
+ * prefix_len i32[B], vis_bits u64[B][Q][W]; lse f32[B][Q][H] (may be NULL);
+ * status i32[B] (OR-ed). A sequence with prefix_len < 0 or
+ * prefix_len + Q > max_pages * page_size gets DDT_ST_CAPACITY, and one with a
+ * page of [0, prefix_len + Q) outside the kv_rows of the cache gets
+ * DDT_ST_RANGE; either way its output is zero and its lse -inf, and nothing
+ * outside its valid pages is read.
+ * DDT_BF16 requires C = 512, R = 64 (tcgen05 kernel), page_size a multiple
+ * of 64 and 16-byte aligned pointers; DDT_F32 takes any C <= 1024, R <= 256.
+ * Both need 1 <= Q <= DDT_MAX_Q. workspace: at least
+ * ddt_verify_attn_workspace_size(dims) bytes of device memory (may be NULL
+ * when that is 0), 256-byte aligned. */
+int ddt_verify_attn(const ddt_attn_dims* dims, const void* q_lat, const void* q_pe,
+                    const void* kv_cache, const int32_t* block_table, const int32_t* prefix_len,
+                    const uint64_t* vis_bits, void* out, float* lse, int32_t* status,
+                    void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* C. Greedy tree accept.
+ * "The Checkpoint", section "The Message" (tree_accept; DDTree greedy
+ * output == AR greedy output) and "The Milestone Commit", section "Mistakes
+ * and Incorrect Assumptions" (the walk carries a safety bound since cyclic
+ * input crashed it).
+ *
+ * Start at the root; at most D times, move to the lowest-slot child c of the
+ * current node (parents[c] == current) whose token equals
+ * target_argmax[current]; stop when there is none. A move to a node already
+ * on the path stops the walk with DDT_ST_CYCLE. bonus = target_argmax at the
+ * last node.
+ * In:  tokens, parents, target_argmax: i32[B][Q] (indexed by tree slot).
+ * Out: accept_idx i32[B][D+1] (slot 0 = root, then the accepted slots, -1
+ *      after), accept_len i32[B] (accepted drafts, root excluded),
+ *      out_tokens i32[B][D+1] (accepted draft tokens, then the bonus, -1
+ *      after), bonus i32[B], status i32[B] (OR-ed).
+ * Limits: 1 <= Q <= DDT_MAX_Q, D >= 0. */
+int ddt_tree_accept(int32_t B, int32_t Q, int32_t D, const int32_t* tokens,
+                    const int32_t* parents, const int32_t* target_argmax, int32_t* accept_idx,
+                    int32_t* accept_len, int32_t* out_tokens, int32_t* bonus, int32_t* status,
+                    cudaStream_t stream);
+
+/* D. Post-verify cache compaction.
+ * "The Checkpoint", section "The Message" (cache append + post-verify
+ * compaction; after accept, gather the accepted-path latents; gather/copy
+ * rows).
+ *
+ * For d = 1..accept_len[b]: the row at slot L + accept_idx[b][d] is copied to
+ * slot L + d (L = prefix_len[b]; the root stays at slot L), with every source
+ * row read before any destination row is written. new_len[b] = L + 1 +
+ * accept_len[b]. kv_cache is [kv_rows][row_bytes] bytes, paged as in
+ * ddt_attn_dims. A sequence whose path or slots fall outside
+ * [0, max_pages * page_size), or whose pages fall outside the kv_rows of the
+ * cache, is left untouched, new_len = L, DDT_ST_RANGE.
+ * Limits: row_bytes a positive multiple of 16, D * row_bytes <= 196608. */
+int ddt_cache_compact(int32_t B, int32_t D, int32_t row_bytes, int32_t page_size,
+                      int32_t max_pages, int64_t kv_rows, void* kv_cache,
+                      const int32_t* block_table,
+                      const int32_t* prefix_len, const int32_t* accept_idx,
+                      const int32_t* accept_len, int32_t* new_len, int32_t* status,
+                      cudaStream_t stream);
+
+/* Everything one verify step reads and writes; see the four calls above for
+ * each array's meaning and layout. tree.B == attn.B and attn.Q ==
+ * tree.budget + 1. target_argmax (i32[B][Q], per tree slot) stands for the
+ * target model's argmax after the verify forward; it must be consistent with
+ * the tree this step builds (the builder is deterministic). */
+typedef struct ddt_step_args {
+  ddt_tree_dims tree;
+  ddt_attn_dims attn;
+  const float* topk_logp;
+  const int32_t* topk_ids;
+  const int32_t* root_tok;
+  const void* q_lat;
+  const void* q_pe;
+  void* kv_cache;
+  const int32_t* block_table;
+  const int32_t* prefix_len;
+  const int32_t* target_argmax;
+  int32_t* tokens;
+  int32_t* parents;
+  int32_t* depths;
+  uint64_t* vis_bits;
+  uint8_t* vis; /* may be NULL */
+  int32_t* first_child;
+  int32_t* next_sibling;
+  int32_t* n_nodes;
+  void* out;
+  float* lse; /* may be NULL */
+  int32_t* accept_idx;
+  int32_t* accept_len;
+  int32_t* out_tokens;
+  int32_t* bonus;
+  int32_t* new_len;
+  int32_t* status;
+  void* workspace;
+  size_t workspace_bytes;
+} ddt_step_args;
+
+/* Bytes of scratch ddt_step needs. */
+size_t ddt_step_workspace_size(const ddt_step_args* args);
+
+/* A -> B -> C+D on `stream`: tree build, verify attention, accept and
+ * compaction (accept and compaction run fused in one kernel). status is
+ * overwritten, then OR-ed by every stage. */
+int ddt_step(const ddt_step_args* args, cudaStream_t stream);
+
+/* Static text for a DDT_E* return code. */
+const char* ddt_strerror(int code);
+
+/* Version of this ABI (increments on any incompatible change). */
+int ddt_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DDT_H_ */

@@ -190,7 +190,7 @@ def slot_rows(block_table_row, page_size: int, slots) -> np.ndarray:
 
 
 def verify_attention(q_lat, q_pe, kv, block_table, prefix_len, vis_bits, scale: float,
-                     page_size: int, rows=None):
+                     page_size: int, rows=None, max_pages=None, with_status=False):
     """Tree-verify MLA-absorb attention in float64.
 
     For sequence ``b``, tree query ``i`` and head ``h``::
@@ -204,7 +204,11 @@ def verify_attention(q_lat, q_pe, kv, block_table, prefix_len, vis_bits, scale: 
     Inputs are upcast to float64 exactly (bf16/fp32 values). ``scale`` is the
     float32 scale the kernels receive. ``rows`` optionally restricts the work
     to a list of ``(b, i)`` pairs (other rows are left as NaN).
-    Returns ``o`` float64 [B, Q, H, C] and ``lse`` float64 [B, Q, H].
+    A sequence with ``L < 0`` or ``L + Q > max_pages * page_size`` gets
+    ``ST_CAPACITY``, one whose pages of ``[0, L + Q)`` fall outside ``kv``
+    gets ``ST_RANGE``; its output is 0 and its lse -inf.
+    Returns ``o`` float64 [B, Q, H, C] and ``lse`` float64 [B, Q, H] (and the
+    per-sequence status when ``with_status``).
     """
     q_lat = np.asarray(q_lat)
     B, Q, H, C = q_lat.shape
@@ -212,9 +216,26 @@ def verify_attention(q_lat, q_pe, kv, block_table, prefix_len, vis_bits, scale: 
     lse = np.full((B, Q, H), np.nan)
     sc = float(np.float32(scale))
     todo = rows if rows is not None else [(b, i) for b in range(B) for i in range(Q)]
+    bt = np.asarray(block_table)
+    if max_pages is None:
+        max_pages = bt.shape[1]
+    status = np.zeros(B, np.int32)
+    n_pages_kv = len(kv) // page_size
+    for b in range(B):
+        L = int(prefix_len[b])
+        if L < 0 or L + Q > max_pages * page_size:
+            status[b] = ST_CAPACITY
+        else:
+            used = bt[b, : -(-(L + Q) // page_size)]
+            if (used < 0).any() or (used >= n_pages_kv).any():
+                status[b] = ST_RANGE
     cache = {}
     for b, i in todo:
         L = int(prefix_len[b])
+        if status[b]:
+            o[b, i] = 0.0
+            lse[b, i] = -np.inf
+            continue
         if b not in cache:
             keys = np.asarray(kv[slot_rows(block_table[b], page_size, np.arange(L + Q))],
                               np.float64)
@@ -230,6 +251,8 @@ def verify_attention(q_lat, q_pe, kv, block_table, prefix_len, vis_bits, scale: 
         l = p.sum(axis=1, keepdims=True)
         o[b, i] = (p @ keys[:, :C]) / l
         lse[b, i] = (m + np.log(l))[:, 0]
+    if with_status:
+        return o, lse, status
     return o, lse
 
 
@@ -289,8 +312,8 @@ def cache_compact(kv, block_table, prefix_len, accept_idx, accept_len, page_size
     to slot ``L + d`` (the root already sits at ``L``); every source row is
     read before any destination row is written. Returns the new cache (a
     copy), ``new_len = L + 1 + accept_len`` and per-sequence status. A
-    sequence whose path or slots fall outside ``[0, max_pages * page_size)``
-    is left untouched with ``ST_RANGE``.
+    sequence whose path or slots fall outside ``[0, max_pages * page_size)``,
+    or whose pages fall outside ``kv``, is left untouched with ``ST_RANGE``.
     """
     new = np.array(kv, copy=True)
     B = len(prefix_len)
@@ -302,9 +325,14 @@ def cache_compact(kv, block_table, prefix_len, accept_idx, accept_len, page_size
         n = int(accept_len[b])
         D = accept_idx.shape[1] - 1
         src_slots = [L + int(accept_idx[b][d]) for d in range(1, n + 1)] if 0 <= n <= D else None
-        if (src_slots is None or L < 0 or L + n >= cap
-                or any(int(accept_idx[b][d]) < 0 for d in range(1, n + 1))
-                or any(s >= cap for s in src_slots)):
+        bad = (src_slots is None or L < 0 or L + n >= cap
+               or any(int(accept_idx[b][d]) < 0 for d in range(1, n + 1))
+               or any(s >= cap for s in src_slots))
+        if not bad:
+            rows_used = slot_rows(block_table[b], page_size,
+                                  src_slots + [L + d for d in range(1, n + 1)]) if n else []
+            bad = any(r < 0 or r >= len(kv) for r in rows_used)
+        if bad:
             status[b] = ST_RANGE
             new_len[b] = L
             continue

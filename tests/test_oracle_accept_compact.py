@@ -174,3 +174,13 @@ def test_qlen1_step_degenerates_to_ar():
     assert res["accept"]["out_tokens"][0][0] == res["target"][0][0]
     np.testing.assert_array_equal(res["kv"], batch.kv)
     assert res["new_len"][0] == batch.prefix_len[0] + 1
+
+
+def test_compaction_page_outside_cache_is_a_range_error():
+    kv = _cache(16, 3, 2)
+    bt = np.array([[0, 7]], np.int32)  # page 7 does not exist (2 pages of 8)
+    new, new_len, st = O.cache_compact(kv, bt, np.array([6], np.int32),
+                                       np.array([[0, 1, 3]], np.int32), np.array([2], np.int32),
+                                       8, 2)
+    assert st[0] == O.ST_RANGE and new_len[0] == 6
+    np.testing.assert_array_equal(new, kv)

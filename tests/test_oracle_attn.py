@@ -130,3 +130,18 @@ def test_scale_is_taken_as_float32():
     _, lse = O.verify_attention(q[..., :C], q[..., C:], phys, bt, np.array([L]), vis, s64, P)
     s = (q[0, 0] @ kv.T) * float(np.float32(s64))
     np.testing.assert_allclose(lse[0, 0], np.log(np.exp(s).sum(1)), rtol=1e-14)
+
+
+def test_capacity_and_page_range_errors_zero_the_sequence():
+    H, C, R, Q = 2, 4, 4, 3
+    g = np.random.default_rng(4)
+    kv = g.standard_normal((32, C + R))
+    q = g.standard_normal((3, Q, H, C + R))
+    bt = np.array([[0, 1], [2, 3], [1, 9]], np.int32)  # page 9 is outside a 4-page cache
+    L = np.array([5, 14, 7], np.int32)  # 14 + 3 > 2 pages * 8 slots; 7 + 3 reaches page 9
+    vis = np.tile(np.array([1, 3, 5], np.uint64).reshape(1, Q, 1), (3, 1, 1))
+    o, lse, st = O.verify_attention(q[..., :C], q[..., C:], kv, bt, L, vis, 0.5, 8,
+                                    with_status=True)
+    assert list(st) == [0, O.ST_CAPACITY, O.ST_RANGE]
+    assert (o[1:] == 0).all() and np.isneginf(lse[1:]).all()
+    assert np.isfinite(o[0]).all()

@@ -1,0 +1,86 @@
+// Internal declarations shared by the translation units of libddt.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ddt.h"
+
+namespace ddt {
+
+constexpr int kMaxQ = DDT_MAX_Q;
+constexpr int kMaxW = (kMaxQ + 63) / 64;
+
+// ---- launchers (defined next to their kernels) ------------------------------
+
+// A. tree build; validates nothing (the ABI layer does).
+cudaError_t launch_tree_build(const ddt_tree_dims& d, const float* topk_logp,
+                              const int32_t* topk_ids, const int32_t* root_tok, int32_t* tokens,
+                              int32_t* parents, int32_t* depths, uint64_t* vis_bits, uint8_t* vis,
+                              int32_t* first_child, int32_t* next_sibling, int32_t* n_nodes,
+                              int32_t* status, cudaStream_t stream);
+
+// C+D. Accept walk and/or compaction in one kernel (one CTA per sequence).
+struct AcceptCompactArgs {
+  int32_t B, Q, D;
+  bool do_accept, do_compact;
+  // accept
+  const int32_t* tokens;
+  const int32_t* parents;
+  const int32_t* target;
+  int32_t* accept_idx;  // in when !do_accept, out otherwise
+  int32_t* accept_len;  // in when !do_accept, out otherwise
+  int32_t* out_tokens;
+  int32_t* bonus;
+  // compaction
+  int32_t row_bytes, page_size, max_pages;
+  int64_t kv_rows;
+  uint8_t* kv;
+  const int32_t* block_table;
+  const int32_t* prefix_len;
+  int32_t* new_len;
+  int32_t* status;
+};
+cudaError_t launch_accept_compact(const AcceptCompactArgs& a, cudaStream_t stream);
+size_t accept_compact_smem_bytes(int32_t D, int32_t row_bytes);
+
+// B. verify attention, fp32 SIMT path (no workspace).
+cudaError_t launch_verify_attn_f32(const ddt_attn_dims& d, const float* q_lat, const float* q_pe,
+                                   const float* kv, const int32_t* block_table,
+                                   const int32_t* prefix_len, const uint64_t* vis_bits, float* out,
+                                   float* lse, int32_t* status, cudaStream_t stream);
+
+// B. verify attention, bf16 tcgen05 path.
+size_t verify_attn_bf16_workspace(const ddt_attn_dims& d);
+cudaError_t launch_verify_attn_bf16(const ddt_attn_dims& d, const void* q_lat, const void* q_pe,
+                                    const void* kv, const int32_t* block_table,
+                                    const int32_t* prefix_len, const uint64_t* vis_bits,
+                                    void* out, float* lse, int32_t* status, void* workspace,
+                                    size_t workspace_bytes, cudaStream_t stream);
+
+// Raise a kernel's dynamic shared-memory limit to `bytes` once per device
+// (later calls, including ones made while a stream is being captured into a
+// CUDA graph, issue no driver call). `done` is the caller's per-kernel cache.
+template <typename Kernel>
+cudaError_t ensure_smem_limit(Kernel k, int bytes, int (&done)[64]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (done[dev] >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[dev] = bytes;
+  return e;
+}
+
+// ---- small device helpers ----------------------------------------------------
+
+__device__ __forceinline__ int64_t slot_row(const int32_t* __restrict__ bt_row, int32_t page_size,
+                                            int64_t slot) {
+  const int64_t page = bt_row[slot / page_size];
+  return page * page_size + slot % page_size;
+}
+
+__device__ __forceinline__ bool warp_any(bool p) { return __any_sync(0xffffffffu, p); }
+
+}  // namespace ddt

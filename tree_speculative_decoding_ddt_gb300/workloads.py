@@ -135,8 +135,10 @@ def rng(cid: int, b: int, stream: int, *extra: int) -> np.random.Generator:
 def to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """float32 -> bfloat16 bit patterns, round to nearest even (NaN kept NaN)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    u = x.view(np.uint32).astype(np.uint64)
-    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    u = x.view(np.uint32)
+    # no uint32 overflow for finite inputs (largest is 0xFF7FFFFF + 0x8000); NaNs are set below
+    with np.errstate(over="ignore"):
+        rounded = (u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
     out = rounded.astype(np.uint16)
     nan = np.isnan(x)
     if nan.any():
