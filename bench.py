@@ -49,7 +49,11 @@ def parse_args(argv=None):
                     help="c1..c4 or a sweep point q<len>_b<batch>_l<prefix>")
     ap.add_argument("--no-graph", action="store_true", help="launch each step directly")
     ap.add_argument("--cpu-seconds", type=float, default=20.0,
-                    help="target CPU time of the oracle baseline sample")
+                    help="target CPU time of the oracle baseline sample (0 = skip it)")
+    ap.add_argument("--attn-steps", type=int, default=None,
+                    help="timed launches of the attention call alone (default steps/4, >= 50)")
+    ap.add_argument("--e2e-steps", type=int, default=None,
+                    help="steps of the end-to-end host-buffer loop (default min(steps, 2000))")
     return ap.parse_args(argv)
 
 
@@ -336,7 +340,7 @@ def run_ours(args):
         bracket_s = time.perf_counter() - t0
         step_ms = [s.elapsed_time(e) for s, e in evs]
         # the dominant kernel, timed the same way
-        n_attn = max(50, args.steps // 4)
+        n_attn = args.attn_steps if args.attn_steps is not None else max(50, args.steps // 4)
         aevs = timed(run["attn"], n_attn)
         torch.cuda.synchronize()
         attn_ms = [s.elapsed_time(e) for s, e in aevs]
@@ -381,13 +385,13 @@ def run_ours(args):
             h.copy_(t, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
-    n_e2e = max(20, min(args.steps, 2000))
-    for _ in range(3):
+    n_e2e = args.e2e_steps if args.e2e_steps is not None else max(20, min(args.steps, 2000))
+    for _ in range(min(3, n_e2e)):
         e2e_step()
     t0 = time.perf_counter()
     for _ in range(n_e2e):
         e2e_step()
-    e2e_s = time.perf_counter() - t0
+    e2e_s = max(time.perf_counter() - t0, 1e-9)
 
     st = buf.status.cpu().numpy()
     if (st & ~DB.ST_BUDGET_PAD).any():
@@ -428,11 +432,12 @@ def run_ours(args):
         },
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
-        "e2e": {"value": world * n_e2e / max_over_ranks(e2e_s, world, dev), "unit": "steps/s",
+        "e2e": {"value": world * max(n_e2e, 1) / max_over_ranks(e2e_s, world, dev),
+                "unit": "steps/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms)},
     }
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
         n_cpu = max(1, int(args.cpu_seconds // 2))
         n, secs = oracle_steps(w, batch, args.cpu_seconds, n_cpu * 50)
         cores, model = cpu_info()

@@ -7,11 +7,12 @@
 // node's ancestor set as a bitmask (parent mask | own bit) and emits the
 // first-child / next-sibling encoding alongside tokens, parents and depths.
 //
-// GB300 layout: one warp per sequence. The frontier lives in shared memory
-// (at most budget+1 live entries, since every pop removes one entry and adds
-// at most two); each pop is a 32-lane argmax over (score desc, depth, rank,
-// parent) followed by two pushes. Node records (score, ancestors, child
-// lists) stay in shared memory and are written out coalesced at the end.
+// GB300 layout: one warp per sequence. The frontier (at most budget+1 live
+// entries, since every pop removes one entry and adds at most two) lives in
+// registers, four entries per lane; each pop is a 32-lane argmax over
+// (score desc, depth, rank, parent) done with three redux.sync reductions on
+// integer keys, followed by two pushes. Node records (score, ancestors,
+// child lists) stay in shared memory and are written out at the end.
 //
 // Two facts keep the shared-memory footprint small without changing the
 // output: a node at depth d is popped at slot >= d, and a node of rank r at
@@ -26,11 +27,10 @@ namespace ddt {
 namespace {
 
 constexpr uint32_t kInvalid = 0xFFFFFFFFu;
+constexpr int kSlots = kMaxQ / 32;  // frontier entries per lane
 
 struct BuildShared {
-  double f_score[kMaxQ];       // frontier: score
-  uint32_t f_key[kMaxQ];       // frontier: depth<<16 | rank<<8 | parent (kInvalid = empty)
-  double n_score[kMaxQ];       // node scores
+  double n_score[kMaxQ];  // node scores
   int32_t n_tok[kMaxQ];
   int32_t n_par[kMaxQ];
   int32_t n_dep[kMaxQ];
@@ -40,13 +40,26 @@ struct BuildShared {
   unsigned long long anc[kMaxQ][kMaxW];
 };
 
-// true when (sa, ka) should pop before (sb, kb); empty entries never win.
-__device__ __forceinline__ bool pops_first(double sa, uint32_t ka, double sb, uint32_t kb) {
-  if (ka == kInvalid) return false;
-  if (kb == kInvalid) return true;
-  if (sa > sb) return true;
-  if (sa < sb) return false;
-  return ka < kb;
+// Order-preserving map of a double to a uint64: a larger score gives a larger
+// key, -0.0 and +0.0 give the same key (they compare equal as doubles).
+// GB300's FP64 pipe is narrow, so all heap comparisons run on these integer
+// keys; only the two score additions per pop stay in FP64 (they must round
+// exactly like the reference's double additions).
+__device__ __forceinline__ unsigned long long score_key(double s) {
+  unsigned long long u = (unsigned long long)__double_as_longlong(s);
+  if (u == 0x8000000000000000ull) u = 0ull;
+  return (u >> 63) ? ~u : (u | 0x8000000000000000ull);
+}
+__device__ __forceinline__ double key_score(unsigned long long k) {
+  const unsigned long long u = (k >> 63) ? (k & 0x7FFFFFFFFFFFFFFFull) : ~k;
+  return __longlong_as_double((long long)u);
+}
+// pop order: larger key first, then smaller tie word (depth<<16|rank<<8|parent)
+__device__ __forceinline__ bool before(unsigned long long ka, uint32_t ta, unsigned long long kb,
+                                       uint32_t tb) {
+  if (ta == kInvalid) return false;
+  if (tb == kInvalid) return true;
+  return ka > kb || (ka == kb && ta < tb);
 }
 
 __global__ void __launch_bounds__(32) k_tree_build(
@@ -86,7 +99,6 @@ __global__ void __launch_bounds__(32) k_tree_build(
     s_ids[e] = ip[d * K + r];
   }
   for (int p = lane; p < kMaxQ; p += 32) {
-    S.f_key[p] = kInvalid;
     S.first_child[p] = -1;
     S.next_sib[p] = -1;
     S.last_child[p] = -1;
@@ -97,48 +109,95 @@ __global__ void __launch_bounds__(32) k_tree_build(
     S.n_par[0] = -1;
     S.n_dep[0] = 0;
     for (int w = 0; w < kMaxW; ++w) S.anc[0][w] = (w == 0) ? 1ull : 0ull;
-    if (!bad && budget > 0) {
-      S.f_score[0] = 0.0 + (double)s_logp[0];
-      S.f_key[0] = (1u << 16) | (0u << 8) | 0u;
-    }
   }
   __syncwarp();
 
-  // ---- pop loop: at most `budget` pops -------------------------------------
+  // ---- frontier: position p lives in lane p % 32, slot p / 32 ---------------
+  unsigned long long fkey[kSlots];
+  uint32_t ftie[kSlots];
+#pragma unroll
+  for (int k = 0; k < kSlots; ++k) {
+    fkey[k] = 0ull;
+    ftie[k] = kInvalid;
+  }
+  if (lane == 0 && !bad && budget > 0) {
+    fkey[0] = score_key(0.0 + (double)s_logp[0]);
+    ftie[0] = (1u << 16) | (0u << 8) | 0u;
+  }
+  unsigned long long bkey = fkey[0];  // this lane's best entry
+  uint32_t btie = ftie[0];
+  int bslot = 0;
+
   int n = 1;
-  int used = 1;  // frontier positions in use (lane 0's view; positions are reused)
+  int used = 1;  // frontier positions handed out so far (positions are reused)
   for (; n < Q && !bad; ++n) {
-    double bs = 0.0;
-    uint32_t bk = kInvalid;
-    int bp = -1;
-#pragma unroll
-    for (int k = 0; k < kMaxQ / 32; ++k) {
-      const int p = lane + 32 * k;
-      const double s = S.f_score[p];
-      const uint32_t key = S.f_key[p];
-      if (pops_first(s, key, bs, bk)) {
-        bs = s;
-        bk = key;
-        bp = p;
-      }
+    // warp argmax in three hardware reductions: key high word, key low word, tie
+    const bool valid = btie != kInvalid;
+    const uint32_t hi = valid ? (uint32_t)(bkey >> 32) : 0u;
+    const uint32_t m1 = __reduce_max_sync(0xffffffffu, hi);
+    const bool c1 = valid && hi == m1;
+    const uint32_t m2 = __reduce_max_sync(0xffffffffu, c1 ? (uint32_t)bkey : 0u);
+    const bool c2 = c1 && (uint32_t)bkey == m2;
+    const uint32_t m3 = __reduce_min_sync(0xffffffffu, c2 ? btie : kInvalid);
+    if (m3 == kInvalid) break;  // candidate tree exhausted
+    const bool winner = c2 && btie == m3;
+
+    const unsigned long long pkey = ((unsigned long long)m1 << 32) | m2;
+    const double ps = key_score(pkey);
+    const int d = (int)(m3 >> 16);
+    const int r = (int)((m3 >> 8) & 0xFFu);
+    const int par = (int)(m3 & 0xFFu);
+
+    // the two pushes (computed by every lane)
+    const bool has_child = d < De;   // rank 0 one level down
+    const bool has_sib = r + 1 < Ke;  // next rank under the same parent
+    unsigned long long ck = 0ull, sk = 0ull;
+    uint32_t ct = kInvalid, st = kInvalid;
+    if (has_child) {
+      ck = score_key(ps + (double)s_logp[d * Ke]);
+      ct = ((uint32_t)(d + 1) << 16) | (uint32_t)n;
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const double os = __shfl_xor_sync(0xffffffffu, bs, off);
-      const uint32_t ok = __shfl_xor_sync(0xffffffffu, bk, off);
-      const int op = __shfl_xor_sync(0xffffffffu, bp, off);
-      if (pops_first(os, ok, bs, bk)) {
-        bs = os;
-        bk = ok;
-        bp = op;
-      }
+    if (has_sib) {
+      sk = score_key(S.n_score[par] + (double)s_logp[(d - 1) * Ke + r + 1]);
+      st = ((uint32_t)d << 16) | ((uint32_t)(r + 1) << 8) | (uint32_t)par;
     }
-    if (bk == kInvalid) break;  // candidate tree exhausted
+    // first push takes the popped position, the second a new one
+    const unsigned long long k1 = has_child ? ck : sk;
+    const uint32_t t1 = has_child ? ct : st;
+    const bool two = has_child && has_sib;
+    if (winner) {
+#pragma unroll
+      for (int k = 0; k < kSlots; ++k)
+        if (k == bslot) {
+          fkey[k] = k1;
+          ftie[k] = t1;
+        }
+    }
+    if (two && lane == (used & 31)) {
+      const int ns = used >> 5;
+#pragma unroll
+      for (int k = 0; k < kSlots; ++k)
+        if (k == ns) {
+          fkey[k] = sk;
+          ftie[k] = st;
+        }
+    }
+    if (winner || (two && lane == (used & 31))) {
+      bkey = 0ull;
+      btie = kInvalid;
+#pragma unroll
+      for (int k = 0; k < kSlots; ++k)
+        if (before(fkey[k], ftie[k], bkey, btie)) {
+          bkey = fkey[k];
+          btie = ftie[k];
+          bslot = k;
+        }
+    }
+    if (two) ++used;
+
+    // node bookkeeping (off the critical path of the next pop)
     if (lane == 0) {
-      const int d = (int)(bk >> 16);
-      const int r = (int)((bk >> 8) & 0xFFu);
-      const int par = (int)(bk & 0xFFu);
-      S.n_score[n] = bs;
+      S.n_score[n] = ps;
       S.n_tok[n] = s_ids[(d - 1) * Ke + r];
       S.n_par[n] = par;
       S.n_dep[n] = d;
@@ -150,24 +209,11 @@ __global__ void __launch_bounds__(32) k_tree_build(
         S.next_sib[S.last_child[par]] = n;
       }
       S.last_child[par] = n;
-      // pushes: the popped position takes the first of them, a new one the second
-      int slot = bp;
-      if (d < De) {  // first child, one level down, rank 0
-        S.f_score[slot] = bs + (double)s_logp[d * Ke];
-        S.f_key[slot] = ((uint32_t)(d + 1) << 16) | (0u << 8) | (uint32_t)n;
-        slot = used++;
-      }
-      if (r + 1 < Ke) {  // next sibling, scored from the parent
-        S.f_score[slot] = S.n_score[par] + (double)s_logp[(d - 1) * Ke + r + 1];
-        S.f_key[slot] = ((uint32_t)d << 16) | ((uint32_t)(r + 1) << 8) | (uint32_t)par;
-        slot = -1;
-      }
-      if (slot == bp) S.f_key[bp] = kInvalid;  // nothing pushed: free the position
-      else if (slot >= 0) --used;             // only the first child was pushed
     }
     __syncwarp();
   }
   const int n_nodes = bad ? 1 : n;
+  __syncwarp();
 
   // ---- write the tree ------------------------------------------------------
   int32_t* tok_o = tokens + (size_t)b * Q;

@@ -187,12 +187,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_KV_FULL + s), 1);
       mbar_init(bar(B_KV_EMPTY + s), 1);
       mbar_init(bar(B_S_FULL + s), 1);
-      mbar_init(bar(B_S_EMPTY + s), 128);
+      mbar_init(bar(B_S_EMPTY + s), 4);  // one arrival per softmax warp
     }
-    mbar_init(bar(B_P_FULL), 128);
+    mbar_init(bar(B_P_FULL), 4);
     mbar_init(bar(B_PV_DONE), 1);
-    mbar_init(bar(B_RECV_FULL), 128);
-    mbar_init(bar(B_SEND_OK), 128);
+    mbar_init(bar(B_RECV_FULL), 1);  // local expect_tx; the peer's bytes complete it
+    mbar_init(bar(B_SEND_OK), 4);    // the peer's softmax warps
     mbar_init(bar(B_MMA_DONE), 1);
     fence_mbar_init();
   }
@@ -310,10 +310,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     const uint32_t recv_local = sbase + OFF_RECV + r * kRecvStride;
     const uint32_t recv_remote = map_peer(recv_local, peer);
-    const uint32_t recv_full_remote = map_peer(bar(B_RECV_FULL), peer);
+    const uint32_t recv_full_remote = map_peer(bar(B_RECV_FULL), peer);  // st.async target
     const uint32_t send_ok_remote = map_peer(bar(B_SEND_OK), peer);
     const uint32_t p_row = sbase + OFF_P + (r >> 3) * 1024 + (r & 7) * 128;
 
+    constexpr uint32_t kRecvBytes = kBM * kBN * 4;  // one partial S tile
+    if (tid == 64) mbar_expect_tx(bar(B_RECV_FULL), kRecvBytes);
     float m_run = -INFINITY, l_run = 0.f;
     for (int jj = 0; jj < nt; ++jj) {
       const int s = jj & 1;
@@ -333,7 +335,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(bar(B_S_EMPTY + s));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_S_EMPTY + s));
 
       // exchange partial scores with the peer CTA (one row per thread)
       if (jj >= 1 &&
@@ -343,13 +346,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int k = 0; k < 16; ++k)
-        st_cluster_v4(recv_remote + 16 * k, sv[4 * k], sv[4 * k + 1], sv[4 * k + 2],
-                      sv[4 * k + 3]);
-      mbar_arrive_cluster(recv_full_remote);
+        st_async_v4(recv_remote + 16 * k, sv[4 * k], sv[4 * k + 1], sv[4 * k + 2],
+                    sv[4 * k + 3], recv_full_remote);
       if (!__all_sync(0xffffffffu, mbar_wait_cluster(bar(B_RECV_FULL), jj & 1))) {
         failed = true;
         break;
       }
+      // arm the next phase before telling the peer it may send again
+      if (tid == 64 && jj + 1 < nt) mbar_expect_tx(bar(B_RECV_FULL), kRecvBytes);
       float x[64];
       const float4* rv = reinterpret_cast<const float4*>(smem + OFF_RECV + r * kRecvStride);
 #pragma unroll
@@ -360,7 +364,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         x[4 * k + 2] = (__uint_as_float(sv[4 * k + 2]) + o4.z) * p.scale_log2;
         x[4 * k + 3] = (__uint_as_float(sv[4 * k + 3]) + o4.w) * p.scale_log2;
       }
-      mbar_arrive_cluster(send_ok_remote);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(send_ok_remote);
 
       // mask: keys past the prefix are visible only along the ancestor path
       if (t0 + kBN > L) {
@@ -375,9 +380,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!vis) x[k] = -INFINITY;
         }
       }
-      float mt = x[0];
+      float mx8[8];
 #pragma unroll
-      for (int k = 1; k < 64; ++k) mt = fmaxf(mt, x[k]);
+      for (int q = 0; q < 8; ++q) mx8[q] = x[q];
+#pragma unroll
+      for (int k = 8; k < 64; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], x[k]);
+      const float mt = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       // lazy rescale: the reference max moves only when the row max passes it by 8 (x2^8)
       float factor = 1.f;
       bool rescale = false;
@@ -388,16 +397,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         m_run = mt;
       }
       uint32_t pk[32];
-      float lsum = 0.f;
+      float ls8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      const float m_use = m_run == -INFINITY ? 0.f : m_run;  // every x is -inf then: p = 0
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
-        const float p0 = m_run == -INFINITY ? 0.f : ex2(x[2 * k] - m_run);
-        const float p1 = m_run == -INFINITY ? 0.f : ex2(x[2 * k + 1] - m_run);
+        const float p0 = ex2(x[2 * k] - m_use);
+        const float p1 = ex2(x[2 * k + 1] - m_use);
         pk[k] = pack_bf16(p0, p1);
         const __nv_bfloat162 pb = *reinterpret_cast<__nv_bfloat162*>(&pk[k]);
-        lsum += __low2float(pb) + __high2float(pb);
+        ls8[k & 7] += __low2float(pb) + __high2float(pb);
       }
-      l_run += lsum;
+      l_run += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
 
       // keys past the end of the sequence in the last tile: zero their values
       // so that 0 * (whatever the page holds) cannot turn into NaN
@@ -443,7 +453,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(B_P_FULL));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_P_FULL));
     }
 
     // ---- epilogue: O half / l ------------------------------------------------
