@@ -12,20 +12,28 @@
 //   S = [q_lat | q_pe] . [c_kv | k_pe]^T   (contraction 576)
 //   O = softmax(S * scale, masked) . c_kv  (output 512)
 // An fp32 O for 128 rows x 512 columns fills all 512 TMEM columns of an SM,
-// leaving nothing for S. So two CTAs of a cluster share one 128-row tile:
-// CTA h owns contraction dims [256h, 256h+256) of c_kv plus [32h, 32h+32) of
-// the rope part, and output dims [256h, 256h+256). Each computes a partial S
-// over its 288 dims on the tensor cores, sends it to its peer through
-// distributed shared memory and adds the peer's; both CTAs then hold the
-// same S bit for bit (fp32 addition commutes), run the same online softmax,
-// and accumulate their own half of O. No FLOP is done twice.
+// and shared memory cannot also hold Q, so one SM cannot own a 128-row tile.
+// Two CTAs of a cluster share it with different roles:
+//   * the S-CTA (cluster rank 0) keeps all of Q in TMEM (288 columns, bf16
+//     pairs), computes S = QK^T for 64 keys at a time (two TMEM S buffers),
+//     runs the online softmax and ships P (bf16, 16 KB per tile) plus the
+//     per-row rescale factors to its peer with one bulk shared-memory copy;
+//   * the O-CTA (rank 1) keeps O (128 x 512 fp32) in TMEM, loads the c_kv
+//     half of each KV tile and accumulates O += P V; its row warps apply the
+//     (rare) rescales and write the output.
+// No FLOP is done twice. The peer-to-peer traffic is P only (bf16, one way),
+// which the cluster link moves in less time than the S-CTA spends on QK^T.
 //
-// Warp roles (192 threads): warp 0 issues TMA loads, warp 1 issues tcgen05
-// MMAs and owns the TMEM allocation, warps 2-5 (one thread per query row)
-// run the softmax and the epilogue. KV tiles of 64 keys are double
-// buffered; S is double buffered in TMEM so the QK^T of tile j+1 runs while
-// the softmax of tile j does. The key range of a sequence can be split over
-// several clusters (split-KV); partial results are merged by k_combine.
+// Warp roles in both CTAs (192 threads): warp 0 issues TMA loads, warp 1
+// issues tcgen05 MMAs and owns the TMEM allocation, warps 2-5 handle one
+// query row per thread. Each CTA fetches a 64-key tile with ONE TMA request
+// (the TMA engine costs about 500 cycles per request whatever its size, so
+// small boxes starve the tensor cores): a 3-D tensor map views the cache as
+// {64 dims, keys, 9 chunks} with strides (row, 128 B), and a box of
+// {64, 64, 9} (S-CTA, 72 KB) or {64, 64, 8} (O-CTA, c_kv only, 64 KB) lands as
+// per-chunk 64-key x 128-byte swizzled tiles. Two stages per CTA. The key
+// range of a sequence can be split over several clusters (split-KV); partial
+// results are merged by k_combine.
 #include <cuda_bf16.h>
 #include <math.h>
 #include <stdio.h>
@@ -46,40 +54,60 @@ constexpr int kC = 512;
 constexpr int kR = 64;
 constexpr int kThreads = 192;
 
-constexpr uint32_t kQChunkBytes = kBM * 128;   // 64 dims x 128 rows, 128-byte swizzle
-constexpr uint32_t kQRopeBytes = kBM * 64;     // 32 dims x 128 rows, 64-byte swizzle
-constexpr uint32_t kKVChunkBytes = kBN * 128;  // 64 dims x 64 keys
-constexpr uint32_t kKVRopeBytes = kBN * 64;    // 32 dims x 64 keys
-constexpr uint32_t kStageBytes = 4 * kKVChunkBytes + kKVRopeBytes;
-constexpr uint32_t kQBytes = 4 * kQChunkBytes + kQRopeBytes;
-constexpr uint32_t kRecvStride = kBN * 4 + 16;  // padded: row r at r * 272 bytes
+constexpr uint32_t kChunkBytes = kBN * 128;             // 64 keys x 64 dims, 128-byte swizzle
+constexpr int kChunksPerTile = (kC + kR) / 64;          // 9 (8 c_kv + 1 rope)
+constexpr uint32_t kTileS = kChunksPerTile * kChunkBytes;  // S-CTA stage: 72 KB
+constexpr uint32_t kTileO = 8 * kChunkBytes;               // O-CTA stage: c_kv, 64 KB
+constexpr uint32_t kHalfBytes = 4 * kChunkBytes;           // 256 c_kv dims x 64 keys
+constexpr int kStages = 2;
+constexpr uint32_t kPBytes = kBM * 128;                 // P tile: 128 rows x 64 keys bf16
+constexpr uint32_t kMsgBytes = kPBytes + kBM * 4 + 16;  // P | per-row factor | 4 warp flags
+constexpr uint32_t kMsgStride = 17408;                  // 1 KB aligned message slots
+constexpr uint32_t kFinBytes = kBM * 4;                 // per-row 1/l
 
-constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_QROPE = 4 * kQChunkBytes;
-constexpr uint32_t OFF_KV = OFF_QROPE + kQRopeBytes;
-constexpr uint32_t OFF_RECV = OFF_KV + 2 * kStageBytes;
-constexpr uint32_t OFF_P = OFF_RECV + kBM * kRecvStride;
-constexpr uint32_t OFF_BAR = OFF_P + kBM * 128;
-constexpr uint32_t kSmemBytes = OFF_BAR + 256 + 1024;  // + alignment slack
-static_assert(OFF_KV % 1024 == 0 && OFF_P % 1024 == 0, "swizzled buffers need 1 KB alignment");
-static_assert(kStageBytes % 1024 == 0, "stage size");
+// S-CTA shared memory
+constexpr uint32_t S_RING = 0;
+constexpr uint32_t S_STAGE = S_RING + kStages * kTileS;  // 2 outgoing messages
+constexpr uint32_t S_FIN = S_STAGE + 2 * kMsgStride;
+constexpr uint32_t S_END = S_FIN + 1024;
+// O-CTA shared memory
+constexpr uint32_t O_RING = 0;
+constexpr uint32_t O_MSG = O_RING + kStages * kTileO;  // 2 incoming messages
+constexpr uint32_t O_FIN = O_MSG + 2 * kMsgStride;
+constexpr uint32_t O_END = O_FIN + 1024;
 
+constexpr uint32_t OFF_BAR = (S_END > O_END ? S_END : O_END);
+constexpr uint32_t kSmemBytes = OFF_BAR + 1024 + 1024;  // barriers + alignment slack
+static_assert(S_STAGE % 1024 == 0 && O_MSG % 1024 == 0 && kMsgStride % 1024 == 0, "alignment");
+static_assert(kMsgBytes <= kMsgStride && kMsgBytes % 16 == 0, "message size");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+
+// mbarriers (indices into one array; each CTA uses its own subset)
 enum Bar {
-  B_Q_FULL = 0,
-  B_KV_FULL = 1,   // +stage
-  B_KV_EMPTY = 3,  // +stage
-  B_S_FULL = 5,    // +buffer
-  B_S_EMPTY = 7,   // +buffer
-  B_P_FULL = 9,
-  B_PV_DONE = 10,
-  B_RECV_FULL = 11,
-  B_SEND_OK = 12,
-  B_MMA_DONE = 13,
-  N_BARS = 14
+  // S-CTA
+  B_RING_FULL = 0,                       // +stage
+  B_RING_EMPTY = B_RING_FULL + kStages,  // +stage
+  B_S_FULL = B_RING_EMPTY + kStages,     // +buffer
+  B_S_EMPTY = B_S_FULL + 2,          // +buffer
+  B_Q_TMEM = B_S_EMPTY + 2,
+  B_P_FREE = B_Q_TMEM + 1,  // +message slot; arrived by the O-CTA
+  // O-CTA
+  B_HALF_FULL = B_P_FREE + 2,            // +stage
+  B_HALF_EMPTY = B_HALF_FULL + kStages,  // +stage
+  B_P_FULL = B_HALF_EMPTY + kStages,     // +message slot; completed by the S-CTA's copy
+  B_O_READY = B_P_FULL + 2,
+  B_PV_DONE = B_O_READY + 1,  // +tile parity
+  B_FIN_FULL = B_PV_DONE + 2,
+  B_TAIL_OK = B_FIN_FULL + 1,
+  // both
+  B_MMA_DONE = B_TAIL_OK + 1,
+  N_BARS = B_MMA_DONE + 1
 };
+static_assert(N_BARS * 8 + 16 <= 1024, "barrier area");
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 256;  // O half at columns [256, 512); S buffers at [0,64), [64,128)
+constexpr uint32_t kTmemQ = 0;    // S-CTA: Q c_kv part [0,256), rope [256,288)
+constexpr uint32_t kTmemS = 384;  // S-CTA: S buffers [384,448), [448,512)
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, kBN, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, true);
@@ -93,6 +121,8 @@ struct Params {
   const int32_t* block_table;
   const int32_t* prefix_len;
   const unsigned long long* vis_bits;
+  const __nv_bfloat16* q_lat;
+  const __nv_bfloat16* q_pe;
   __nv_bfloat16* out;
   float* lse;
   int32_t* status;
@@ -105,35 +135,65 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// rows of this CTA's half written as zero (capacity/range errors, empty splits)
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src_cta,
+                                                  uint32_t bytes, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst_cluster),
+      "r"(src_cta), "r"(bytes), "r"(bar_cluster)
+      : "memory");
+}
+
+__device__ __forceinline__ void row_barrier() {  // the 128 row threads (warps 2-5)
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+// Same barrier, returning the AND of `ok` over the 128 row threads, so that a
+// bounded wait that gave up in one warp makes all four leave together.
+__device__ __forceinline__ bool row_barrier_and(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.and.pred po, 1, 128, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)ok)
+      : "memory");
+  return r != 0;
+}
+
+// rows of this unit written as empty (capacity/range errors, empty splits):
+// the O-CTA writes zero output, the S-CTA writes lse = -inf
 __device__ void write_empty(const Params& p, int b, int rt, int sp, uint32_t rank) {
   const int QH = p.Q * p.H;
   const long long total = (long long)p.B * QH;
-  for (int e = threadIdx.x; e < kBM * 32; e += kThreads) {
-    const int r = e >> 5, c = e & 31;  // 32 chunks of 8 columns per half row
-    const int lr = (int)rt * kBM + r;
+  for (int e = threadIdx.x; e < kBM * 64; e += kThreads) {
+    const int r = e >> 6, c = e & 63;  // 64 chunks of 8 columns per row
+    const int lr = rt * kBM + r;
     if (lr >= QH) continue;
     const long long grow = (long long)b * QH + lr;
-    if (p.n_split == 1) {
-      reinterpret_cast<uint4*>(p.out + grow * kC + 256 * rank)[c] = make_uint4(0, 0, 0, 0);
-      if (rank == 0 && c == 0 && p.lse) p.lse[grow] = -INFINITY;
-    } else {
-      float4* dst = reinterpret_cast<float4*>(p.part_o + ((long long)sp * total + grow) * kC +
-                                              256 * rank);
-      dst[2 * c] = make_float4(0.f, 0.f, 0.f, 0.f);
-      dst[2 * c + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (rank == 0 && c == 0) p.part_lse[(long long)sp * total + grow] = -INFINITY;
+    if (rank == 1) {
+      if (p.n_split == 1) {
+        reinterpret_cast<uint4*>(p.out + grow * kC)[c] = make_uint4(0, 0, 0, 0);
+      } else {
+        float4* dst = reinterpret_cast<float4*>(p.part_o + ((long long)sp * total + grow) * kC);
+        dst[2 * c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        dst[2 * c + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    } else if (c == 0) {
+      if (p.n_split == 1) {
+        if (p.lse) p.lse[grow] = -INFINITY;
+      } else {
+        p.part_lse[(long long)sp * total + grow] = -INFINITY;
+      }
     }
   }
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    k_verify_attn_bf16(const __grid_constant__ CUtensorMap tm_kv_c,
-                       const __grid_constant__ CUtensorMap tm_kv_r,
-                       const __grid_constant__ CUtensorMap tm_q_c,
-                       const __grid_constant__ CUtensorMap tm_q_r, const Params p) {
+    k_verify_attn_bf16(const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_o,
+                       const Params p) {
   extern __shared__ __align__(1024) unsigned char smem_dyn[];
-  // 1 KB alignment for the swizzled tiles
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -141,7 +201,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + N_BARS * 8);
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
-  const uint32_t rank = cluster_rank();
+  const uint32_t rank = cluster_rank();  // 0: S-CTA, 1: O-CTA
   const uint32_t peer = rank ^ 1u;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -182,17 +242,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   // ---- setup ---------------------------------------------------------------
   if (tid == 0) {
-    mbar_init(bar(B_Q_FULL), 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(B_KV_FULL + s), 1);
-      mbar_init(bar(B_KV_EMPTY + s), 1);
-      mbar_init(bar(B_S_FULL + s), 1);
-      mbar_init(bar(B_S_EMPTY + s), 4);  // one arrival per softmax warp
+    if (rank == 0) {
+      for (int s = 0; s < kStages; ++s) {
+        mbar_init(bar(B_RING_FULL + s), 1);
+        mbar_init(bar(B_RING_EMPTY + s), 1);
+      }
+      for (int s = 0; s < 2; ++s) {
+        mbar_init(bar(B_S_FULL + s), 1);
+        mbar_init(bar(B_S_EMPTY + s), 4);
+        mbar_init(bar(B_P_FREE + s), 1);
+      }
+      mbar_init(bar(B_Q_TMEM), 4);
+    } else {
+      for (int s = 0; s < kStages; ++s) {
+        mbar_init(bar(B_HALF_FULL + s), 1);
+        mbar_init(bar(B_HALF_EMPTY + s), 1);
+      }
+      for (int s = 0; s < 2; ++s) mbar_init(bar(B_P_FULL + s), 1);
+      mbar_init(bar(B_O_READY), 4);
+      mbar_init(bar(B_PV_DONE + 0), 1);
+      mbar_init(bar(B_PV_DONE + 1), 1);
+      mbar_init(bar(B_FIN_FULL), 1);
+      mbar_init(bar(B_TAIL_OK), 1);
+      // arm the incoming messages 0 and 1 and the final 1/l vector
+      mbar_expect_tx(bar(B_P_FULL + 0), kMsgBytes);
+      if (nt > 1) mbar_expect_tx(bar(B_P_FULL + 1), kMsgBytes);
+      mbar_expect_tx(bar(B_FIN_FULL), kFinBytes);
     }
-    mbar_init(bar(B_P_FULL), 4);
-    mbar_init(bar(B_PV_DONE), 1);
-    mbar_init(bar(B_RECV_FULL), 1);  // local expect_tx; the peer's bytes complete it
-    mbar_init(bar(B_SEND_OK), 4);    // the peer's softmax warps
     mbar_init(bar(B_MMA_DONE), 1);
     fence_mbar_init();
   }
@@ -204,303 +280,391 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  cluster_sync();  // the peer's barriers are initialised before any remote arrive
+  cluster_sync();  // the peer's barriers are initialised before any remote operation
 
   bool failed = false;
   const long long row0 = (long long)b * QH + (long long)rt * kBM;
+  auto krow_of = [&](int jj) -> long long {
+    const long long t0 = (long long)(j_begin + jj) * kBN;
+    return (long long)bt[t0 / p.page_size] * p.page_size + t0 % p.page_size;
+  };
 
-  if (warp == 0) {
-    // ======================= TMA producer =======================
-    if (lane == 0) {
-      prefetch_tmap(&tm_kv_c);
-      prefetch_tmap(&tm_kv_r);
-      mbar_expect_tx(bar(B_Q_FULL), kQBytes);
-      for (int c = 0; c < 4; ++c)
-        tma_load_2d(sbase + OFF_Q + c * kQChunkBytes, &tm_q_c, 256 * rank + 64 * c, (int)row0,
-                    bar(B_Q_FULL));
-      tma_load_2d(sbase + OFF_QROPE, &tm_q_r, 32 * rank, (int)row0, bar(B_Q_FULL));
-      int issued = 0;
-      for (int jj = 0; jj < nt; ++jj) {
-        const int s = jj & 1;
-        if (jj >= 2 && !mbar_wait(bar(B_KV_EMPTY + s), ((jj >> 1) - 1) & 1)) {
-          failed = true;
-          break;
-        }
-        const long long t0 = (long long)(j_begin + jj) * kBN;
-        const long long krow = (long long)bt[t0 / p.page_size] * p.page_size + t0 % p.page_size;
-        const uint32_t st = sbase + OFF_KV + s * kStageBytes;
-        mbar_expect_tx(bar(B_KV_FULL + s), kStageBytes);
-        for (int c = 0; c < 4; ++c)
-          tma_load_2d(st + c * kKVChunkBytes, &tm_kv_c, 256 * rank + 64 * c, (int)krow,
-                      bar(B_KV_FULL + s));
-        tma_load_2d(st + 4 * kKVChunkBytes, &tm_kv_r, kC + 32 * rank, (int)krow,
-                    bar(B_KV_FULL + s));
-        ++issued;
-      }
-      // no copy may still be landing in shared memory when the CTA leaves
-      for (int jj = max(0, issued - 2); jj < issued; ++jj)
-        if (!mbar_wait(bar(B_KV_FULL + (jj & 1)), (jj >> 1) & 1)) failed = true;
-      if (!mbar_wait(bar(B_Q_FULL), 0)) failed = true;
-    }
-  } else if (warp == 1) {
-    // ======================= MMA issuer =======================
-    if (lane == 0) {
-      const uint32_t p_desc_base = sbase + OFF_P;
-      auto issue_pv = [&](int t) -> bool {
-        if (!mbar_wait(bar(B_P_FULL), t & 1)) return false;
-        tc_fence_after();
-        const uint32_t st = sbase + OFF_KV + (t & 1) * kStageBytes;
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t ad = smem_desc(p_desc_base + kk * 32, 16, 1024, kSwizzle128B);
-          const uint64_t bd = smem_desc(st + kk * 2048, kKVChunkBytes, 1024, kSwizzle128B);
-          umma_bf16(tmem + kTmemO, ad, bd, kIdescPV, (t > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(bar(B_PV_DONE));
-        umma_commit(bar(B_KV_EMPTY + (t & 1)));
-        return true;
-      };
-      if (!mbar_wait(bar(B_Q_FULL), 0)) failed = true;
-      for (int jj = 0; jj < nt && !failed; ++jj) {
-        const int s = jj & 1;
-        if (!mbar_wait(bar(B_KV_FULL + s), (jj >> 1) & 1)) { failed = true; break; }
-        if (jj >= 2 && !mbar_wait(bar(B_S_EMPTY + s), ((jj >> 1) - 1) & 1)) { failed = true; break; }
-        tc_fence_after();
-        const uint32_t st = sbase + OFF_KV + s * kStageBytes;
-        const uint32_t d = tmem + s * kBN;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad =
-                smem_desc(sbase + OFF_Q + c * kQChunkBytes + kk * 32, 16, 1024, kSwizzle128B);
-            const uint64_t bd =
-                smem_desc(st + c * kKVChunkBytes + kk * 32, 16, 1024, kSwizzle128B);
-            umma_bf16(d, ad, bd, kIdescS, (c | kk) ? 1u : 0u);
+  if (rank == 0) {
+    // ========================= S-CTA =========================
+    if (warp == 0) {
+      if (lane == 0) {  // TMA: one 72 KB request per tile
+        prefetch_tmap(&tm_s);
+        int u = 0;
+        for (; u < nt; ++u) {
+          const int slot = u % kStages;
+          if (u >= kStages && !mbar_wait(bar(B_RING_EMPTY + slot), ((u / kStages) - 1) & 1)) {
+            failed = true;
+            break;
           }
+          mbar_expect_tx(bar(B_RING_FULL + slot), kTileS);
+          tma_load_3d(sbase + S_RING + slot * kTileS, &tm_s, 0, (int)krow_of(u), 0,
+                      bar(B_RING_FULL + slot));
         }
+        for (int v = max(0, u - kStages); v < u; ++v)  // nothing may land after the CTA leaves
+          if (!mbar_wait(bar(B_RING_FULL + v % kStages), (v / kStages) & 1)) failed = true;
+      }
+    } else if (warp == 1) {
+      if (lane == 0) {  // QK^T: A = Q from TMEM, B = KV chunk (K-major)
+        if (!mbar_wait(bar(B_Q_TMEM), 0)) failed = true;
+        tc_fence_after();
+        for (int jj = 0; jj < nt && !failed; ++jj) {
+          const int sb = jj & 1;
+          if (jj >= 2 && !mbar_wait(bar(B_S_EMPTY + sb), ((jj >> 1) - 1) & 1)) {
+            failed = true;
+            break;
+          }
+          const uint32_t d = tmem + kTmemS + sb * kBN;
+          const int slot = jj % kStages;
+          if (!mbar_wait(bar(B_RING_FULL + slot), (jj / kStages) & 1)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = sbase + S_RING + slot * kTileS;
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-          const uint64_t ad = smem_desc(sbase + OFF_QROPE + kk * 32, 16, 512, kSwizzle64B);
-          const uint64_t bd = smem_desc(st + 4 * kKVChunkBytes + kk * 32, 16, 512, kSwizzle64B);
-          umma_bf16(d, ad, bd, kIdescS, 1u);
+          for (int c = 0; c < kChunksPerTile; ++c) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t bd = smem_desc(st + c * kChunkBytes + kk * 32, 16, 1024, kSwizzle128B);
+              umma_bf16_ts(d, tmem + kTmemQ + 32 * c + 8 * kk, bd, kIdescS, (c | kk) ? 1u : 0u);
+            }
+          }
+          umma_commit(bar(B_RING_EMPTY + slot));
+          umma_commit(bar(B_S_FULL + sb));
         }
-        umma_commit(bar(B_S_FULL + s));
-        if (jj >= 1 && !issue_pv(jj - 1)) { failed = true; break; }
+        umma_commit(bar(B_MMA_DONE));
+        if (!mbar_wait(bar(B_MMA_DONE), 0)) failed = true;
       }
-      if (!failed && !issue_pv(nt - 1)) failed = true;
-      // every MMA issued above has completed before TMEM is released
-      umma_commit(bar(B_MMA_DONE));
-      if (!mbar_wait(bar(B_MMA_DONE), 0)) failed = true;
-    }
-  } else {
-    // ======================= softmax + epilogue =======================
-    const int qd = warp & 3;
-    const int r = qd * 32 + lane;
-    const uint32_t t_lane = tmem + ((uint32_t)(qd * 32) << 16);
-    const int lr = rt * kBM + r;
-    const bool row_ok = lr < QH;
-    const int qi = row_ok ? lr / p.H : 0;
-    const int W = (p.Q + 63) >> 6;
-    unsigned long long vis0 = 0ull, vis1 = 0ull;
-    if (row_ok) {
-      const unsigned long long* vb = p.vis_bits + ((size_t)b * p.Q + qi) * W;
-      vis0 = vb[0];
-      if (W > 1) vis1 = vb[1];
-    }
-    const uint32_t recv_local = sbase + OFF_RECV + r * kRecvStride;
-    const uint32_t recv_remote = map_peer(recv_local, peer);
-    const uint32_t recv_full_remote = map_peer(bar(B_RECV_FULL), peer);  // st.async target
-    const uint32_t send_ok_remote = map_peer(bar(B_SEND_OK), peer);
-    const uint32_t p_row = sbase + OFF_P + (r >> 3) * 1024 + (r & 7) * 128;
-
-    constexpr uint32_t kRecvBytes = kBM * kBN * 4;  // one partial S tile
-    if (tid == 64) mbar_expect_tx(bar(B_RECV_FULL), kRecvBytes);
-    float m_run = -INFINITY, l_run = 0.f;
-    for (int jj = 0; jj < nt; ++jj) {
-      const int s = jj & 1;
-      const long long t0 = (long long)(j_begin + jj) * kBN;
-      // waits are made warp-uniform: the tcgen05 loads below are warp-collective
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S_FULL + s), (jj >> 1) & 1))) {
-        failed = true;
-        break;
+    } else {
+      // ---------------- softmax (one query row per thread) ----------------
+      const int qd = warp & 3;
+      const int r = qd * 32 + lane;
+      const uint32_t t_lane = tmem + ((uint32_t)(qd * 32) << 16);
+      const int lr = rt * kBM + r;
+      const bool row_ok = lr < QH;
+      const int qi = row_ok ? lr / p.H : 0;
+      const int W = (p.Q + 63) >> 6;
+      unsigned long long vis0 = 0ull, vis1 = 0ull;
+      if (row_ok) {
+        const unsigned long long* vb = p.vis_bits + ((size_t)b * p.Q + qi) * W;
+        vis0 = vb[0];
+        if (W > 1) vis1 = vb[1];
       }
-      tc_fence_after();
-      uint32_t sv[64];
+      // Q row r -> TMEM columns [0,288) as bf16 pairs (rows past the sequence: 0)
       {
-        uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[0]);
-        uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32]);
-        tmem_ld32(t_lane + s * kBN, lo);
-        tmem_ld32(t_lane + s * kBN + 32, hi);
-      }
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_S_EMPTY + s));
-
-      // exchange partial scores with the peer CTA (one row per thread)
-      if (jj >= 1 &&
-          !__all_sync(0xffffffffu, mbar_wait_cluster(bar(B_SEND_OK), (jj - 1) & 1))) {
-        failed = true;
-        break;
-      }
-#pragma unroll
-      for (int k = 0; k < 16; ++k)
-        st_async_v4(recv_remote + 16 * k, sv[4 * k], sv[4 * k + 1], sv[4 * k + 2],
-                    sv[4 * k + 3], recv_full_remote);
-      if (!__all_sync(0xffffffffu, mbar_wait_cluster(bar(B_RECV_FULL), jj & 1))) {
-        failed = true;
-        break;
-      }
-      // arm the next phase before telling the peer it may send again
-      if (tid == 64 && jj + 1 < nt) mbar_expect_tx(bar(B_RECV_FULL), kRecvBytes);
-      float x[64];
-      const float4* rv = reinterpret_cast<const float4*>(smem + OFF_RECV + r * kRecvStride);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float4 o4 = rv[k];
-        x[4 * k + 0] = (__uint_as_float(sv[4 * k + 0]) + o4.x) * p.scale_log2;
-        x[4 * k + 1] = (__uint_as_float(sv[4 * k + 1]) + o4.y) * p.scale_log2;
-        x[4 * k + 2] = (__uint_as_float(sv[4 * k + 2]) + o4.z) * p.scale_log2;
-        x[4 * k + 3] = (__uint_as_float(sv[4 * k + 3]) + o4.w) * p.scale_log2;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(send_ok_remote);
-
-      // mask: keys past the prefix are visible only along the ancestor path
-      if (t0 + kBN > L) {
-#pragma unroll
-        for (int k = 0; k < 64; ++k) {
-          const long long slot = t0 + k;
-          bool vis = slot < L;
-          if (!vis && slot < n_keys) {
-            const int t = (int)(slot - L);
-            vis = ((t < 64 ? vis0 : vis1) >> (t & 63)) & 1ull;
-          }
-          if (!vis) x[k] = -INFINITY;
-        }
-      }
-      float mx8[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) mx8[q] = x[q];
-#pragma unroll
-      for (int k = 8; k < 64; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], x[k]);
-      const float mt = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      // lazy rescale: the reference max moves only when the row max passes it by 8 (x2^8)
-      float factor = 1.f;
-      bool rescale = false;
-      if (mt > m_run + 8.f) {
-        factor = ex2(m_run - mt);  // 0 when m_run is -inf
-        l_run *= factor;
-        rescale = jj > 0;
-        m_run = mt;
-      }
-      uint32_t pk[32];
-      float ls8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      const float m_use = m_run == -INFINITY ? 0.f : m_run;  // every x is -inf then: p = 0
-#pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const float p0 = ex2(x[2 * k] - m_use);
-        const float p1 = ex2(x[2 * k + 1] - m_use);
-        pk[k] = pack_bf16(p0, p1);
-        const __nv_bfloat162 pb = *reinterpret_cast<__nv_bfloat162*>(&pk[k]);
-        ls8[k & 7] += __low2float(pb) + __high2float(pb);
-      }
-      l_run += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
-
-      // keys past the end of the sequence in the last tile: zero their values
-      // so that 0 * (whatever the page holds) cannot turn into NaN
-      if (t0 + kBN > n_keys && r < kBN && t0 + r >= n_keys) {
-        const uint32_t st = OFF_KV + s * kStageBytes;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint4* rowp = reinterpret_cast<uint4*>(smem + st + c * kKVChunkBytes +
-                                                 (r >> 3) * 1024 + (r & 7) * 128);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) rowp[q] = make_uint4(0, 0, 0, 0);
-        }
-      }
-      // P buffer and O are free once PV of the previous tile has completed
-      if (jj >= 1) {
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_PV_DONE), (jj - 1) & 1))) {
-          failed = true;
-          break;
-        }
-        tc_fence_after();
-      }
-      // rows that keep their reference max multiply by 1; the TMEM round trip
-      // is done by the whole warp whenever any of its rows needs it
-      if (__any_sync(0xffffffffu, rescale)) {
-        if (!rescale) factor = 1.f;
+        const uint4* src = reinterpret_cast<const uint4*>(p.q_lat + (row0 + r) * kC);
+        const uint4* srp = reinterpret_cast<const uint4*>(p.q_pe + (row0 + r) * kR);
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(t_lane + kTmemO + 32 * c, ov);
-          tmem_ld_wait();
+        for (int c = 0; c < kChunksPerTile; ++c) {
+          uint32_t v[32];
 #pragma unroll
-          for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * factor);
-          tmem_st32(t_lane + kTmemO + 32 * c, ov);
+          for (int q = 0; q < 8; ++q) {
+            uint4 x = make_uint4(0, 0, 0, 0);
+            if (row_ok) x = c < 8 ? src[8 * c + q] : srp[q];
+            v[4 * q + 0] = x.x;
+            v[4 * q + 1] = x.y;
+            v[4 * q + 2] = x.z;
+            v[4 * q + 3] = x.w;
+          }
+          tmem_st32(t_lane + kTmemQ + 32 * c, v);
         }
         tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_Q_TMEM));
       }
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t addr = p_row + ((uint32_t)(c ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * c]),
-                     "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
-                     : "memory");
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_P_FULL));
-    }
+      const uint32_t msg_peer0 = map_peer(sbase + O_MSG, peer);
+      const uint32_t pfull_peer0 = map_peer(bar(B_P_FULL), peer);
 
-    // ---- epilogue: O half / l ------------------------------------------------
-    if (!__all_sync(0xffffffffu, !failed && mbar_wait(bar(B_PV_DONE), (nt - 1) & 1)))
-      failed = true;
-    if (!failed) {
-      tc_fence_after();
-      const bool live = l_run > 0.f;
-      const float inv_l = live ? 1.f / l_run : 0.f;
-      const float lse_v = live ? (m_run + __log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
-      const long long grow = row0 + r;
-#pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
-        uint32_t ov[32];
-        tmem_ld32(t_lane + kTmemO + 32 * c, ov);
-        tmem_ld_wait();
-        if (!row_ok) continue;
-        if (p.n_split == 1) {
-          uint4* dst = reinterpret_cast<uint4*>(p.out + grow * kC + 256 * rank + 32 * c);
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int jj = 0; jj < nt; ++jj) {
+        const int sb = jj & 1;
+        const long long t0 = (long long)(j_begin + jj) * kBN;
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_S_FULL + sb), (jj >> 1) & 1));
+        if (!row_barrier_and(ok)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        float x[64];
+        {
+          uint32_t sv[32];
+          tmem_ld32(t_lane + kTmemS + sb * kBN, sv);
+          tmem_ld_wait();
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            dst[q] = make_uint4(pack_bf16(__uint_as_float(ov[8 * q + 0]) * inv_l,
-                                          __uint_as_float(ov[8 * q + 1]) * inv_l),
-                                pack_bf16(__uint_as_float(ov[8 * q + 2]) * inv_l,
-                                          __uint_as_float(ov[8 * q + 3]) * inv_l),
-                                pack_bf16(__uint_as_float(ov[8 * q + 4]) * inv_l,
-                                          __uint_as_float(ov[8 * q + 5]) * inv_l),
-                                pack_bf16(__uint_as_float(ov[8 * q + 6]) * inv_l,
-                                          __uint_as_float(ov[8 * q + 7]) * inv_l));
+          for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(sv[k]) * p.scale_log2;
+          tmem_ld32(t_lane + kTmemS + sb * kBN + 32, sv);
+          tmem_ld_wait();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) x[32 + k] = __uint_as_float(sv[k]) * p.scale_log2;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_S_EMPTY + sb));
+
+        // mask: keys past the prefix are visible only along the ancestor path
+        if (t0 + kBN > L) {
+#pragma unroll
+          for (int k = 0; k < 64; ++k) {
+            const long long slot = t0 + k;
+            bool vis = slot < L;
+            if (!vis && slot < n_keys) {
+              const int t = (int)(slot - L);
+              vis = ((t < 64 ? vis0 : vis1) >> (t & 63)) & 1ull;
+            }
+            if (!vis) x[k] = -INFINITY;
           }
-        } else {
-          float4* dst = reinterpret_cast<float4*>(
-              p.part_o + ((long long)sp * total_rows + grow) * kC + 256 * rank + 32 * c);
+        }
+        float mx8[8];
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            dst[q] = make_float4(__uint_as_float(ov[4 * q + 0]) * inv_l,
-                                 __uint_as_float(ov[4 * q + 1]) * inv_l,
-                                 __uint_as_float(ov[4 * q + 2]) * inv_l,
-                                 __uint_as_float(ov[4 * q + 3]) * inv_l);
+        for (int q = 0; q < 8; ++q) mx8[q] = x[q];
+#pragma unroll
+        for (int k = 8; k < 64; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], x[k]);
+        const float mt = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        // lazy rescale: the reference max moves only when the row max passes it
+        // by 8 (a factor 2^8); O on the peer is then multiplied by `factor`
+        float factor = 1.f;
+        bool rescale = false;
+        if (mt > m_run + 8.f) {
+          factor = ex2(m_run - mt);  // 0 when m_run is -inf
+          l_run *= factor;
+          rescale = jj > 0;
+          m_run = mt;
+        }
+        uint32_t pk[32];
+        float ls8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        const float m_use = m_run == -INFINITY ? 0.f : m_run;  // every x is -inf then: p = 0
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float p0 = ex2(x[2 * k] - m_use);
+          const float p1 = ex2(x[2 * k + 1] - m_use);
+          pk[k] = pack_bf16(p0, p1);
+          const __nv_bfloat162 pb = *reinterpret_cast<__nv_bfloat162*>(&pk[k]);
+          ls8[k & 7] += __low2float(pb) + __high2float(pb);
+        }
+        l_run += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+
+        // outgoing message jj % 2 (and the peer's slot) are free once the peer
+        // has finished PV of tile jj-2
+        const int mb = jj & 1;
+        ok = jj < 2 ||
+             __all_sync(0xffffffffu, mbar_wait_cluster(bar(B_P_FREE + mb), ((jj >> 1) - 1) & 1));
+        if (!row_barrier_and(ok)) {
+          failed = true;
+          break;
+        }
+        unsigned char* msg = smem + S_STAGE + mb * kMsgStride;
+        const uint32_t msg_s = sbase + S_STAGE + mb * kMsgStride;
+        const uint32_t p_row = msg_s + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t addr = p_row + ((uint32_t)(c ^ (r & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * c]),
+                       "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
+                       : "memory");
+        }
+        reinterpret_cast<float*>(msg + kPBytes)[r] = rescale ? factor : 1.f;
+        const bool any_rescale = __any_sync(0xffffffffu, rescale);
+        if (lane == 0) reinterpret_cast<uint32_t*>(msg + kPBytes + kBM * 4)[qd] = any_rescale;
+        fence_proxy_async_smem();
+        row_barrier();
+        if (tid == 64)
+          bulk_copy_to_peer(msg_peer0 + mb * kMsgStride, msg_s, kMsgBytes, pfull_peer0 + 8 * mb);
+      }
+
+      // ---- finish: lse here, 1/l to the peer --------------------------------
+      if (!failed) {
+        const bool live = l_run > 0.f;
+        const long long grow = row0 + r;
+        if (row_ok) {
+          const float lse_v =
+              live ? (m_run + __log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
+          if (p.n_split == 1) {
+            if (p.lse) p.lse[grow] = lse_v;
+          } else {
+            p.part_lse[(long long)sp * total_rows + grow] = lse_v;
+          }
+        }
+        reinterpret_cast<float*>(smem + S_FIN)[r] = live ? 1.f / l_run : 0.f;
+        fence_proxy_async_smem();
+      }
+      row_barrier();
+      if (tid == 64 && !failed)
+        bulk_copy_to_peer(map_peer(sbase + O_FIN, peer), sbase + S_FIN, kFinBytes,
+                          map_peer(bar(B_FIN_FULL), peer));
+    }
+  } else {
+    // ========================= O-CTA =========================
+    if (warp == 0) {
+      if (lane == 0) {  // TMA: one 64 KB request (the c_kv part) per tile
+        prefetch_tmap(&tm_o);
+        int u = 0;
+        for (; u < nt; ++u) {
+          const int slot = u % kStages;
+          if (u >= kStages && !mbar_wait(bar(B_HALF_EMPTY + slot), ((u / kStages) - 1) & 1)) {
+            failed = true;
+            break;
+          }
+          mbar_expect_tx(bar(B_HALF_FULL + slot), kTileO);
+          tma_load_3d(sbase + O_RING + slot * kTileO, &tm_o, 0, (int)krow_of(u), 0,
+                      bar(B_HALF_FULL + slot));
+        }
+        for (int v = max(0, u - kStages); v < u; ++v)
+          if (!mbar_wait(bar(B_HALF_FULL + v % kStages), (v / kStages) & 1)) failed = true;
+        // keys past the end of the sequence in the last tile: zero their values
+        // so that 0 * (whatever the page holds) cannot turn into NaN
+        if (!failed && u == nt) {
+          const long long t0 = (long long)(j_begin + nt - 1) * kBN;
+          if (t0 + kBN > n_keys) {
+            unsigned char* base = smem + O_RING + ((nt - 1) % kStages) * kTileO;
+            for (int rr = (int)(n_keys - t0); rr < kBN; ++rr)
+              for (int c = 0; c < 8; ++c) {
+                uint4* row = reinterpret_cast<uint4*>(base + c * kChunkBytes + (rr >> 3) * 1024 +
+                                                      (rr & 7) * 128);
+                for (int q = 0; q < 8; ++q) row[q] = make_uint4(0, 0, 0, 0);
+              }
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(bar(B_TAIL_OK));
         }
       }
-      if (row_ok && rank == 0) {
-        if (p.n_split == 1) {
-          if (p.lse) p.lse[grow] = lse_v;
-        } else {
-          p.part_lse[(long long)sp * total_rows + grow] = lse_v;
+    } else if (warp == 1) {
+      if (lane == 0) {  // PV: A = P (K-major, from the S-CTA), B = V half (MN-major)
+        int n_flag = 0;
+        for (int jj = 0; jj < nt && !failed; ++jj) {
+          const int mb = jj & 1;
+          if (!mbar_wait_cluster(bar(B_P_FULL + mb), (jj >> 1) & 1)) {
+            failed = true;
+            break;
+          }
+          const unsigned char* msg = smem + O_MSG + mb * kMsgStride;
+          const uint4 fl = *reinterpret_cast<const uint4*>(msg + kPBytes + kBM * 4);
+          if (jj > 0 && (fl.x | fl.y | fl.z | fl.w)) {  // row warps rescale O first
+            if (!mbar_wait(bar(B_O_READY), n_flag & 1)) {
+              failed = true;
+              break;
+            }
+            ++n_flag;
+          }
+          const int slot = jj % kStages;
+          if (!mbar_wait(bar(B_HALF_FULL + slot), (jj / kStages) & 1) ||
+              (jj == nt - 1 && !mbar_wait(bar(B_TAIL_OK), 0))) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t pa = sbase + O_MSG + mb * kMsgStride;
+          const uint32_t h0 = sbase + O_RING + slot * kTileO;
+          const uint32_t h1 = h0 + kHalfBytes;
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            const uint64_t ad = smem_desc(pa + kk * 32, 16, 1024, kSwizzle128B);
+            const uint32_t acc = (jj > 0 || kk > 0) ? 1u : 0u;
+            umma_bf16(tmem, ad, smem_desc(h0 + kk * 2048, kChunkBytes, 1024, kSwizzle128B),
+                      kIdescPV, acc);
+            umma_bf16(tmem + 256, ad,
+                      smem_desc(h1 + kk * 2048, kChunkBytes, 1024, kSwizzle128B), kIdescPV, acc);
+          }
+          umma_commit(bar(B_PV_DONE + (jj & 1)));
+          umma_commit(bar(B_HALF_EMPTY + slot));
+        }
+        umma_commit(bar(B_MMA_DONE));
+        if (!mbar_wait(bar(B_MMA_DONE), 0)) failed = true;
+      }
+    } else {
+      // ---------------- row warps: rescales, message slot recycling, output ---
+      const int qd = warp & 3;
+      const int r = qd * 32 + lane;
+      const uint32_t t_lane = tmem + ((uint32_t)(qd * 32) << 16);
+      const int lr = rt * kBM + r;
+      const bool row_ok = lr < QH;
+      const uint32_t pfree_peer0 = map_peer(bar(B_P_FREE), peer);
+      for (int jj = 0; jj < nt; ++jj) {
+        const int mb = jj & 1;
+        bool ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar(B_P_FULL + mb), (jj >> 1) & 1));
+        if (!row_barrier_and(ok)) {
+          failed = true;
+          break;
+        }
+        const unsigned char* msg = smem + O_MSG + mb * kMsgStride;
+        const uint4 fl = *reinterpret_cast<const uint4*>(msg + kPBytes + kBM * 4);
+        if (jj > 0 && (fl.x | fl.y | fl.z | fl.w)) {
+          const float f = reinterpret_cast<const float*>(msg + kPBytes)[r];
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(B_PV_DONE + ((jj - 1) & 1)), ((jj - 1) >> 1) & 1));
+          if (!row_barrier_and(ok)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < 16; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(t_lane + 32 * c, ov);
+            tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * f);
+            tmem_st32(t_lane + 32 * c, ov);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_O_READY));
+        }
+        // slot mb is free once PV of tile jj has completed; all row warps move
+        // on together so that no warp can fall a message behind
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(B_PV_DONE + mb), (jj >> 1) & 1));
+        if (!row_barrier_and(ok)) {
+          failed = true;
+          break;
+        }
+        if (tid == 64) {
+          if (jj + 2 < nt) mbar_expect_tx(bar(B_P_FULL + mb), kMsgBytes);
+          mbar_arrive_cluster(pfree_peer0 + 8 * mb);
+        }
+      }
+      // ---- epilogue: O / l ------------------------------------------------------
+      if (!__all_sync(0xffffffffu, !failed && mbar_wait_cluster(bar(B_FIN_FULL), 0) &&
+                                       mbar_wait(bar(B_PV_DONE + ((nt - 1) & 1)),
+                                                 ((nt - 1) >> 1) & 1)))
+        failed = true;
+      if (!failed) {
+        tc_fence_after();
+        const float inv_l = reinterpret_cast<const float*>(smem + O_FIN)[r];
+        const long long grow = row0 + r;
+#pragma unroll 1
+        for (int c = 0; c < 16; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(t_lane + 32 * c, ov);
+          tmem_ld_wait();
+          if (!row_ok) continue;
+          if (p.n_split == 1) {
+            uint4* dst = reinterpret_cast<uint4*>(p.out + grow * kC + 32 * c);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(pack_bf16(__uint_as_float(ov[8 * q + 0]) * inv_l,
+                                            __uint_as_float(ov[8 * q + 1]) * inv_l),
+                                  pack_bf16(__uint_as_float(ov[8 * q + 2]) * inv_l,
+                                            __uint_as_float(ov[8 * q + 3]) * inv_l),
+                                  pack_bf16(__uint_as_float(ov[8 * q + 4]) * inv_l,
+                                            __uint_as_float(ov[8 * q + 5]) * inv_l),
+                                  pack_bf16(__uint_as_float(ov[8 * q + 6]) * inv_l,
+                                            __uint_as_float(ov[8 * q + 7]) * inv_l));
+          } else {
+            float4* dst = reinterpret_cast<float4*>(
+                p.part_o + ((long long)sp * total_rows + grow) * kC + 32 * c);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[q] = make_float4(__uint_as_float(ov[4 * q + 0]) * inv_l,
+                                   __uint_as_float(ov[4 * q + 1]) * inv_l,
+                                   __uint_as_float(ov[4 * q + 2]) * inv_l,
+                                   __uint_as_float(ov[4 * q + 3]) * inv_l);
+          }
         }
       }
     }
@@ -512,7 +676,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  cluster_sync();  // no remote store or arrive may target a CTA that has left
+  cluster_sync();  // every copy and remote arrive between the two CTAs has landed
 }
 
 // Merge of the split-KV partials: o = sum_s w_s o_s / sum_s w_s with
@@ -616,18 +780,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return fn;
 }
 
-bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
-               uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows,
-               CUtensorMapSwizzle swz) {
+bool encode_kv_3d(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_chunks) {
   auto fn = encoder();
   if (fn == nullptr) return false;
-  cuuint64_t dims[2] = {inner, rows};
-  cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {box_inner, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  cuuint64_t dims[3] = {64, rows, (cuuint64_t)kChunksPerTile};
+  cuuint64_t strides[2] = {(cuuint64_t)(kC + kR) * 2, 128};
+  cuuint32_t box[3] = {64, (cuuint32_t)kBN, box_chunks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -649,15 +811,10 @@ cudaError_t launch_verify_attn_bf16(const ddt_attn_dims& d, const void* q_lat, c
   const long long rows = (long long)d.B * d.Q * d.H;
   if (d.kv_rows < 1 || rows > 0x7fffffffLL || d.kv_rows > 0x7fffffffLL)
     return cudaErrorInvalidValue;
-  CUtensorMap tm_kv_c, tm_kv_r, tm_q_c, tm_q_r;
-  const uint64_t row_kv = (kC + kR) * 2;
-  if (!encode_2d(&tm_kv_c, kv, kC + kR, (uint64_t)d.kv_rows, row_kv, 64, kBN,
-                 CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&tm_kv_r, kv, kC + kR, (uint64_t)d.kv_rows, row_kv, 32, kBN,
-                 CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !encode_2d(&tm_q_c, q_lat, kC, (uint64_t)rows, kC * 2, 64, kBM,
-                 CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&tm_q_r, q_pe, kR, (uint64_t)rows, kR * 2, 32, kBM, CU_TENSOR_MAP_SWIZZLE_64B))
+  // the cache as {64 dims, rows, 9 chunks} with strides (row, 128 B)
+  CUtensorMap tm_s, tm_o;
+  if (!encode_kv_3d(&tm_s, kv, (uint64_t)d.kv_rows, kChunksPerTile) ||
+      !encode_kv_3d(&tm_o, kv, (uint64_t)d.kv_rows, 8))
     return cudaErrorInvalidValue;
 
   Params p;
@@ -667,6 +824,8 @@ cudaError_t launch_verify_attn_bf16(const ddt_attn_dims& d, const void* q_lat, c
   p.n_rt = pl.n_rt; p.n_split = pl.n_split;
   p.block_table = block_table; p.prefix_len = prefix_len;
   p.vis_bits = reinterpret_cast<const unsigned long long*>(vis_bits);
+  p.q_lat = static_cast<const __nv_bfloat16*>(q_lat);
+  p.q_pe = static_cast<const __nv_bfloat16*>(q_pe);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse; p.status = status;
   p.part_o = nullptr; p.part_lse = nullptr;
@@ -678,7 +837,7 @@ cudaError_t launch_verify_attn_bf16(const ddt_attn_dims& d, const void* q_lat, c
   cudaError_t e = ensure_smem_limit(k_verify_attn_bf16, (int)kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
   k_verify_attn_bf16<<<(unsigned)(pl.units * 2), kThreads, kSmemBytes, stream>>>(
-      tm_kv_c, tm_kv_r, tm_q_c, tm_q_r, p);
+      tm_s, tm_o, p);
   e = cudaGetLastError();
   if (e != cudaSuccess || pl.n_split == 1) return e;
   k_combine<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(rows, pl.n_split, p.part_o,
