@@ -155,8 +155,8 @@ size_t ddt_verify_attn_workspace_size(const ddt_attn_dims* dims);
  * page of [0, prefix_len + Q) outside the kv_rows of the cache gets
  * DDT_ST_RANGE; either way its output is zero and its lse -inf, and nothing
  * outside its valid pages is read.
- * DDT_BF16 requires C = 512, R = 64 (tcgen05 kernel), page_size a multiple
- * of 64 and 16-byte aligned pointers; DDT_F32 takes any C <= 1024, R <= 256.
+ * DDT_BF16 requires C = 512, R = 64 (tcgen05 kernel), scale > 0, page_size a
+ * multiple of 64 and 16-byte aligned pointers; DDT_F32 takes any C <= 1024, R <= 256.
  * Both need 1 <= Q <= DDT_MAX_Q. workspace: at least
  * ddt_verify_attn_workspace_size(dims) bytes of device memory (may be NULL
  * when that is 0), 256-byte aligned. */
@@ -164,6 +164,26 @@ int ddt_verify_attn(const ddt_attn_dims* dims, const void* q_lat, const void* q_
                     const void* kv_cache, const int32_t* block_table, const int32_t* prefix_len,
                     const uint64_t* vis_bits, void* out, float* lse, int32_t* status,
                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* B'. The bf16 verify attention of ddt_verify_attn, for callers that cannot
+ * allocate device memory. This entry point has no counterpart on the source
+ * pages; it exists for code that can hand the library its inputs and outputs
+ * but cannot obtain scratch memory (device allocation forbidden or
+ * unavailable where it runs, e.g. a plugin given only its I/O buffers, or a
+ * loop that must never enter an allocator).
+ * Same arguments and results as ddt_verify_attn with dims->dtype == DDT_BF16,
+ * minus the workspace: the split-KV scratch comes from a fixed 32 MiB array
+ * the library reserves on every GPU that loads it (held until exit). Returns
+ * DDT_EWORKSPACE, before enqueuing anything, when these dims need more
+ * scratch than that (ddt_verify_attn_workspace_size(dims) > 32 MiB), and
+ * DDT_EUNSUPPORTED for DDT_F32. All calls share the array: calls whose GPU
+ * work may overlap (several streams or host threads) race and must be
+ * serialised by the caller. The first call on a device looks up the array's
+ * address with that device current; make it before any stream capture. */
+int ddt_verify_attn_noalloc(const ddt_attn_dims* dims, const void* q_lat, const void* q_pe,
+                            const void* kv_cache, const int32_t* block_table,
+                            const int32_t* prefix_len, const uint64_t* vis_bits, void* out,
+                            float* lse, int32_t* status, cudaStream_t stream);
 
 /* C. Greedy tree accept.
  * "The Checkpoint", section "The Message" (tree_accept; DDTree greedy

@@ -62,6 +62,7 @@ SIGNATURES = {
     "ddt_verify_attn_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(AttnDims)]),
     "ddt_verify_attn": (ctypes.c_int, [ctypes.POINTER(AttnDims)] + [_P] * 10 +
                         [ctypes.c_size_t, _P]),
+    "ddt_verify_attn_noalloc": (ctypes.c_int, [ctypes.POINTER(AttnDims)] + [_P] * 10),
     "ddt_tree_accept": (ctypes.c_int, [ctypes.c_int32] * 3 + [_P] * 9),
     "ddt_cache_compact": (ctypes.c_int, [ctypes.c_int32] * 5 + [ctypes.c_int64] + [_P] * 8),
     "ddt_step_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(StepArgs)]),
@@ -194,6 +195,38 @@ def ddt_verify_attn(q_lat, q_pe, kv_cache, block_table, prefix_len, vis_bits, sc
                                 workspace.numel() if workspace is not None else 0,
                                 _stream(stream))
     _check("ddt_verify_attn", rc)
+    return out, lse, status
+
+
+def ddt_verify_attn_noalloc(q_lat, q_pe, kv_cache, block_table, prefix_len, vis_bits,
+                            scale: float, page_size: int, max_len: int, out=None, lse=None,
+                            status=None, stream=None):
+    """B'. :func:`ddt_verify_attn` (bf16 only) with the split-KV scratch taken
+    from the library's fixed device array instead of a caller workspace, for
+    callers that cannot allocate device memory. Calls that may overlap on the
+    GPU share that array and must be serialised. Returns (out, lse, status)."""
+    B, Q, H, C = q_lat.shape
+    R = q_pe.shape[-1]
+    _need(q_lat, "q_lat", torch.bfloat16)
+    _need(q_pe, "q_pe", torch.bfloat16, (B, Q, H, R))
+    _need(kv_cache, "kv_cache", torch.bfloat16)
+    _need(block_table, "block_table", torch.int32)
+    _need(prefix_len, "prefix_len", torch.int32, (B,))
+    _need(vis_bits, "vis_bits", torch.int64, (B, Q, (Q + 63) // 64))
+    dev = q_lat.device
+    dims = attn_dims(B, Q, H, C, R, page_size, block_table.shape[1], kv_cache.shape[0], DDT_BF16,
+                     scale, max_len)
+    if out is None:
+        out = torch.empty((B, Q, H, C), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, Q, H), dtype=torch.float32, device=dev)
+    if status is None:
+        status = torch.zeros((B,), dtype=torch.int32, device=dev)
+    rc = load().ddt_verify_attn_noalloc(ctypes.byref(dims), _ptr(q_lat), _ptr(q_pe),
+                                        _ptr(kv_cache), _ptr(block_table), _ptr(prefix_len),
+                                        _ptr(vis_bits), _ptr(out), _ptr(lse), _ptr(status),
+                                        _stream(stream))
+    _check("ddt_verify_attn_noalloc", rc)
     return out, lse, status
 
 

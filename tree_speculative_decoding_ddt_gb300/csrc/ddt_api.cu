@@ -31,7 +31,8 @@ int check_attn_dims(const ddt_attn_dims* d) {
   if (d->dtype == DDT_F32) {
     if (d->C > 1024 || d->R > 256) return DDT_EUNSUPPORTED;
   } else if (d->dtype == DDT_BF16) {
-    if (d->C != 512 || d->R != 64 || d->page_size % 64 != 0) return DDT_EUNSUPPORTED;
+    if (d->C != 512 || d->R != 64 || d->page_size % 64 != 0 || !(d->scale > 0.f))
+      return DDT_EUNSUPPORTED;
   } else {
     return DDT_EINVAL;
   }
@@ -91,6 +92,20 @@ int run_attn(const ddt_attn_dims* d, const void* q_lat, const void* q_pe, const 
 }
 
 }  // namespace
+
+namespace ddt {
+// Host checks of a verify-attention call (dims, then pointers and alignment),
+// shared with entry points defined in other files.
+int check_verify_attn_args(const ddt_attn_dims* d, const void* q_lat, const void* q_pe,
+                           const void* kv, const int32_t* block_table, const int32_t* prefix_len,
+                           const uint64_t* vis_bits, const void* out, const int32_t* status) {
+  int rc = check_attn_dims(d);
+  if (rc) return rc;
+  if (!q_lat || !q_pe || !kv || !block_table || !prefix_len || !vis_bits || !out || !status)
+    return DDT_EINVAL;
+  return DDT_OK;
+}
+}  // namespace ddt
 
 extern "C" {
 

@@ -58,6 +58,11 @@ cudaError_t launch_verify_attn_bf16(const ddt_attn_dims& d, const void* q_lat, c
                                     void* out, float* lse, int32_t* status, void* workspace,
                                     size_t workspace_bytes, cudaStream_t stream);
 
+// Host checks of a verify-attention call (defined in ddt_api.cu).
+int check_verify_attn_args(const ddt_attn_dims* d, const void* q_lat, const void* q_pe,
+                           const void* kv, const int32_t* block_table, const int32_t* prefix_len,
+                           const uint64_t* vis_bits, const void* out, const int32_t* status);
+
 // Raise a kernel's dynamic shared-memory limit to `bytes` once per device
 // (later calls, including ones made while a stream is being captured into a
 // CUDA graph, issue no driver call). `done` is the caller's per-kernel cache.

@@ -135,6 +135,24 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Packed fp32 pair arithmetic (one instruction for two lanes of work).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
 __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src_cta,
                                                   uint32_t bytes, uint32_t bar_cluster) {
   asm volatile(
@@ -284,8 +302,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   bool failed = false;
   const long long row0 = (long long)b * QH + (long long)rt * kBM;
+  // Row tiles of a sequence walk its key tiles from staggered starting points
+  // (all clusters reading the same tile at once contend for the same L2
+  // lines); the unit's last tile, which holds the sequence tail, stays last.
+  // The online softmax does not depend on the order.
+  const int nrot = nt - 1;
+  const int rot = nrot > 0 ? (int)(((long long)rt * nrot) / p.n_rt) : 0;
+  auto tile_of = [&](int jj) -> int {
+    return (jj == nt - 1) ? j_begin + jj : j_begin + (jj + rot) % nrot;
+  };
   auto krow_of = [&](int jj) -> long long {
-    const long long t0 = (long long)(j_begin + jj) * kBN;
+    const long long t0 = (long long)tile_of(jj) * kBN;
     return (long long)bt[t0 / p.page_size] * p.page_size + t0 % p.page_size;
   };
 
@@ -381,27 +408,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t msg_peer0 = map_peer(sbase + O_MSG, peer);
       const uint32_t pfull_peer0 = map_peer(bar(B_P_FULL), peer);
 
+      const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
       float m_run = -INFINITY, l_run = 0.f;
       for (int jj = 0; jj < nt; ++jj) {
         const int sb = jj & 1;
-        const long long t0 = (long long)(j_begin + jj) * kBN;
+        const long long t0 = (long long)tile_of(jj) * kBN;
         bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_S_FULL + sb), (jj >> 1) & 1));
         if (!row_barrier_and(ok)) {
           failed = true;
           break;
         }
         tc_fence_after();
-        float x[64];
+        float x[64];  // raw scores q.k (the scale is applied inside the exponent)
         {
-          uint32_t sv[32];
-          tmem_ld32(t_lane + kTmemS + sb * kBN, sv);
+          uint32_t sa[32], sc[32];
+          tmem_ld32(t_lane + kTmemS + sb * kBN, sa);
+          tmem_ld32(t_lane + kTmemS + sb * kBN + 32, sc);
           tmem_ld_wait();
 #pragma unroll
-          for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(sv[k]) * p.scale_log2;
-          tmem_ld32(t_lane + kTmemS + sb * kBN + 32, sv);
-          tmem_ld_wait();
-#pragma unroll
-          for (int k = 0; k < 32; ++k) x[32 + k] = __uint_as_float(sv[k]) * p.scale_log2;
+          for (int k = 0; k < 32; ++k) {
+            x[k] = __uint_as_float(sa[k]);
+            x[32 + k] = __uint_as_float(sc[k]);
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -425,8 +453,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 8; ++q) mx8[q] = x[q];
 #pragma unroll
         for (int k = 8; k < 64; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], x[k]);
+        // the scale is positive, so it commutes with the max
         const float mt = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
+                         p.scale_log2;
         // lazy rescale: the reference max moves only when the row max passes it
         // by 8 (a factor 2^8); O on the peer is then multiplied by `factor`
         float factor = 1.f;
@@ -438,17 +468,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           m_run = mt;
         }
         uint32_t pk[32];
-        float ls8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        const float m_use = m_run == -INFINITY ? 0.f : m_run;  // every x is -inf then: p = 0
+        // p = 2^(x * scale*log2(e) - m); every x is -inf while m is -inf: p = 0
+        const float nm = m_run == -INFINITY ? 0.f : -m_run;
+        const float2 neg_m = make_float2(nm, nm);
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          const float p0 = ex2(x[2 * k] - m_use);
-          const float p1 = ex2(x[2 * k + 1] - m_use);
-          pk[k] = pack_bf16(p0, p1);
-          const __nv_bfloat162 pb = *reinterpret_cast<__nv_bfloat162*>(&pk[k]);
-          ls8[k & 7] += __low2float(pb) + __high2float(pb);
+          const float2 e = ffma2(make_float2(x[2 * k], x[2 * k + 1]), sl2, neg_m);
+          const float2 pp = make_float2(ex2(e.x), ex2(e.y));
+          pk[k] = pack_bf16(pp.x, pp.y);
+          acc[k & 3] = fadd2(acc[k & 3], pp);
         }
-        l_run += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+        const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
+        const float2 a = fadd2(a01, a23);
+        l_run += a.x + a.y;
 
         // outgoing message jj % 2 (and the peer's slot) are free once the peer
         // has finished PV of tile jj-2
