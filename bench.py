@@ -83,6 +83,30 @@ def measured_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one
+# k_verify_attn_bf16 launch, from ncu captures of the kernel built from the
+# source whose sha256 is given; reported as null once that source changes.
+MEASURED_TRAFFIC = {
+    "c2_max_budget": ("274bc41f00b6ce50dbd03f0af2f36b02f9d0f3fd8f982357e6c07fbfc6ad82ae",
+                      9772544),
+    "c4_deep_long": ("274bc41f00b6ce50dbd03f0af2f36b02f9d0f3fd8f982357e6c07fbfc6ad82ae",
+                     556023808 + 116403712),
+}
+
+
+def measured_traffic(w):
+    """ncu DRAM bytes per launch of the attention kernel for workload w, or
+    None when none was taken for the current kernel source."""
+    import hashlib
+    entry = MEASURED_TRAFFIC.get(w.name)
+    if entry is None:
+        return None
+    src = os.path.join(ROOT, "tree_speculative_decoding_ddt_gb300", "csrc", "verify_attn_bf16.cu")
+    with open(src, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()
+    return entry[1] if digest == entry[0] else None
+
+
 def attn_work(w, prefix_len, depths, dtype_bytes):
     """Algorithmic FLOPs and bytes of one verify-attention launch: every
     visible (query row, key) pair costs 2(C+R) for q.k and 2C for p.v; a
@@ -425,7 +449,8 @@ def run_ours(args):
             "unit": "TFLOP/s" if bound == "tensor" else "GB/s",
             "frac": (achieved_tf / tf) if bound == "tensor" else (achieved_gb / hbm),
             "peak_source": f"{src} (MEASURED_PEAKS.json burst)" if src == "measured" else src,
-            "traffic": None,
+            "traffic": measured_traffic(w) if bf16 else None,
+            "traffic_kernel": "k_verify_attn_bf16 (ncu, one launch)",
             "algorithmic_flops": flops, "algorithmic_bytes": byt,
             "attn_us": attn_s * 1e6, "roofline_us": t_roof * 1e6,
             "frac_of_roofline_time": t_roof / attn_s,
