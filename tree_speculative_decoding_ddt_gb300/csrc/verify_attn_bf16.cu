@@ -24,16 +24,20 @@
 // No FLOP is done twice. The peer-to-peer traffic is P only (bf16, one way),
 // which the cluster link moves in less time than the S-CTA spends on QK^T.
 //
-// Warp roles in both CTAs (192 threads): warp 0 issues TMA loads, warp 1
-// issues tcgen05 MMAs and owns the TMEM allocation, warps 2-5 handle one
-// query row per thread. Each CTA fetches a 64-key tile with ONE TMA request
-// (the TMA engine costs about 500 cycles per request whatever its size, so
-// small boxes starve the tensor cores): a 3-D tensor map views the cache as
-// {64 dims, keys, 9 chunks} with strides (row, 128 B), and a box of
-// {64, 64, 9} (S-CTA, 72 KB) or {64, 64, 8} (O-CTA, c_kv only, 64 KB) lands as
-// per-chunk 64-key x 128-byte swizzled tiles. Two stages per CTA. The key
-// range of a sequence can be split over several clusters (split-KV); partial
-// results are merged by k_combine.
+// Warp roles (224 threads): warp 0 issues TMA loads; warp 1 owns the TMEM
+// allocation and issues tcgen05 MMAs; warps 2-5 handle one query row per
+// thread; in the S-CTA warp 6 is a second MMA issuer (a single thread issues
+// an MMA only about every 50 cycles, slower than an N=64 MMA runs, so the two
+// issuers take alternate key tiles). Q reaches the S-CTA by TMA (staged in
+// the ring, then copied to TMEM by the row warps). Each CTA fetches a 64-key
+// tile with ONE TMA request (the TMA engine costs about 500 cycles per
+// request whatever its size, so small boxes starve the tensor cores): a 3-D
+// tensor map views the cache as {64 dims, keys, 9 chunks} with strides (row,
+// 128 B), and a box of {64, 64, 9} (S-CTA, 72 KB) or {64, 64, 8} (O-CTA, c_kv
+// only, 64 KB) lands as per-chunk 64-key x 128-byte swizzled tiles. Two
+// stages per CTA. The O-CTA writes its output rows through shared memory with
+// one bulk copy per row. The key range of a sequence can be split over
+// several clusters (split-KV); partial results are merged by k_combine.
 #include <cuda_bf16.h>
 #include <math.h>
 #include <stdio.h>
@@ -52,7 +56,7 @@ constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 64;   // keys per KV tile
 constexpr int kC = 512;
 constexpr int kR = 64;
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 
 constexpr uint32_t kChunkBytes = kBN * 128;             // 64 keys x 64 dims, 128-byte swizzle
 constexpr int kChunksPerTile = (kC + kR) / 64;          // 9 (8 c_kv + 1 rope)
@@ -64,6 +68,8 @@ constexpr uint32_t kPBytes = kBM * 128;                 // P tile: 128 rows x 64
 constexpr uint32_t kMsgBytes = kPBytes + kBM * 4 + 16;  // P | per-row factor | 4 warp flags
 constexpr uint32_t kMsgStride = 17408;                  // 1 KB aligned message slots
 constexpr uint32_t kFinBytes = kBM * 4;                 // per-row 1/l
+constexpr uint32_t kQBytes = kBM * (kC + kR) * 2;       // Q tile: 128 rows x 576 bf16
+constexpr uint32_t kOutStride = 1040;                   // staged output row: 1 KB + 16 B
 
 // S-CTA shared memory
 constexpr uint32_t S_RING = 0;
@@ -81,6 +87,8 @@ constexpr uint32_t kSmemBytes = OFF_BAR + 1024 + 1024;  // barriers + alignment 
 static_assert(S_STAGE % 1024 == 0 && O_MSG % 1024 == 0 && kMsgStride % 1024 == 0, "alignment");
 static_assert(kMsgBytes <= kMsgStride && kMsgBytes % 16 == 0, "message size");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+static_assert(kQBytes <= kStages * kTileS, "the Q tile is staged in the S-CTA ring");
+static_assert(kBM * kOutStride <= O_FIN, "the output is staged in the O-CTA ring and messages");
 
 // mbarriers (indices into one array; each CTA uses its own subset)
 enum Bar {
@@ -90,7 +98,8 @@ enum Bar {
   B_S_FULL = B_RING_EMPTY + kStages,     // +buffer
   B_S_EMPTY = B_S_FULL + 2,          // +buffer
   B_Q_TMEM = B_S_EMPTY + 2,
-  B_P_FREE = B_Q_TMEM + 1,  // +message slot; arrived by the O-CTA
+  B_Q_FULL = B_Q_TMEM + 1,  // Q tile landed in the ring (TMA)
+  B_P_FREE = B_Q_FULL + 1,  // +message slot; arrived by the O-CTA
   // O-CTA
   B_HALF_FULL = B_P_FREE + 2,            // +stage
   B_HALF_EMPTY = B_HALF_FULL + kStages,  // +stage
@@ -210,7 +219,8 @@ __device__ void write_empty(const Params& p, int b, int rt, int sp, uint32_t ran
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     k_verify_attn_bf16(const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_o,
-                       const Params p) {
+                       const __grid_constant__ CUtensorMap tm_ql,
+                       const __grid_constant__ CUtensorMap tm_qp, const Params p) {
   extern __shared__ __align__(1024) unsigned char smem_dyn[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
@@ -271,6 +281,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(bar(B_P_FREE + s), 1);
       }
       mbar_init(bar(B_Q_TMEM), 4);
+      mbar_init(bar(B_Q_FULL), 1);
+      mbar_init(bar(B_MMA_DONE), 2);  // one commit per MMA issuer
     } else {
       for (int s = 0; s < kStages; ++s) {
         mbar_init(bar(B_HALF_FULL + s), 1);
@@ -286,8 +298,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_expect_tx(bar(B_P_FULL + 0), kMsgBytes);
       if (nt > 1) mbar_expect_tx(bar(B_P_FULL + 1), kMsgBytes);
       mbar_expect_tx(bar(B_FIN_FULL), kFinBytes);
+      mbar_init(bar(B_MMA_DONE), 1);
     }
-    mbar_init(bar(B_MMA_DONE), 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -304,12 +316,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const long long row0 = (long long)b * QH + (long long)rt * kBM;
   // Row tiles of a sequence walk its key tiles from staggered starting points
   // (all clusters reading the same tile at once contend for the same L2
-  // lines); the unit's last tile, which holds the sequence tail, stays last.
-  // The online softmax does not depend on the order.
-  const int nrot = nt - 1;
+  // lines). Only tiles that lie wholly in the prefix rotate; the tiles that
+  // hold tree keys come last, in order, so that the running max is taken
+  // over full prefix tiles before the sparse, masked tree tiles (a walk that
+  // starts on a tile with a handful of visible keys rescales O again and
+  // again), and the unit's last tile, which holds the sequence tail, stays
+  // last. The online softmax does not depend on the order.
+  const int n_pure = (int)(L / kBN);  // tiles with no tree key
+  const int nrot = max(0, min(j_begin + nt, n_pure) - j_begin);
   const int rot = nrot > 0 ? (int)(((long long)rt * nrot) / p.n_rt) : 0;
   auto tile_of = [&](int jj) -> int {
-    return (jj == nt - 1) ? j_begin + jj : j_begin + (jj + rot) % nrot;
+    return (jj < nrot) ? j_begin + (jj + rot) % nrot : j_begin + jj;
   };
   auto krow_of = [&](int jj) -> long long {
     const long long t0 = (long long)tile_of(jj) * kBN;
@@ -319,10 +336,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (rank == 0) {
     // ========================= S-CTA =========================
     if (warp == 0) {
-      if (lane == 0) {  // TMA: one 72 KB request per tile
+      if (lane == 0) {
         prefetch_tmap(&tm_s);
+        // Q (128 rows: 8 chunks of c_kv dims, then the rope part) lands in the
+        // ring first; the row warps move it to TMEM, then the ring takes K
+        mbar_expect_tx(bar(B_Q_FULL), kQBytes);
+        tma_load_3d(sbase + S_RING, &tm_ql, 0, (int)row0, 0, bar(B_Q_FULL));
+        tma_load_2d(sbase + S_RING + 8 * kBM * 128, &tm_qp, 0, (int)row0, bar(B_Q_FULL));
         int u = 0;
-        for (; u < nt; ++u) {
+        // K may overwrite the ring once Q is in TMEM; the Q copy has always
+        // landed before anything else is issued (or the CTA leaves)
+        if (!mbar_wait(bar(B_Q_TMEM), 0)) failed = true;
+        if (!mbar_wait(bar(B_Q_FULL), 0)) failed = true;
+        for (; u < nt && !failed; ++u) {  // one 72 KB request per tile
           const int slot = u % kStages;
           if (u >= kStages && !mbar_wait(bar(B_RING_EMPTY + slot), ((u / kStages) - 1) & 1)) {
             failed = true;
@@ -335,11 +361,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int v = max(0, u - kStages); v < u; ++v)  // nothing may land after the CTA leaves
           if (!mbar_wait(bar(B_RING_FULL + v % kStages), (v / kStages) & 1)) failed = true;
       }
-    } else if (warp == 1) {
-      if (lane == 0) {  // QK^T: A = Q from TMEM, B = KV chunk (K-major)
+    } else if (warp == 1 || warp == 6) {
+      // QK^T: A = Q from TMEM, B = KV chunk (K-major). One thread issues a
+      // tcgen05.mma about every 50 cycles, while an N=64 MMA runs in 32, so
+      // two issuers take alternate tiles (and own S buffer / ring slot
+      // tile & 1) to keep the tensor pipe full.
+      if (lane == 0) {
+        const int first = warp == 1 ? 0 : 1;
         if (!mbar_wait(bar(B_Q_TMEM), 0)) failed = true;
         tc_fence_after();
-        for (int jj = 0; jj < nt && !failed; ++jj) {
+        for (int jj = first; jj < nt && !failed; jj += 2) {
           const int sb = jj & 1;
           if (jj >= 2 && !mbar_wait(bar(B_S_EMPTY + sb), ((jj >> 1) - 1) & 1)) {
             failed = true;
@@ -382,17 +413,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         vis0 = vb[0];
         if (W > 1) vis1 = vb[1];
       }
-      // Q row r -> TMEM columns [0,288) as bf16 pairs (rows past the sequence: 0)
-      {
-        const uint4* src = reinterpret_cast<const uint4*>(p.q_lat + (row0 + r) * kC);
-        const uint4* srp = reinterpret_cast<const uint4*>(p.q_pe + (row0 + r) * kR);
+      // Q row r -> TMEM columns [0,288) as bf16 pairs, from the TMA-staged
+      // tile (chunk c: 128 rows x 128 B, 16-byte units swizzled by row & 7).
+      // Rows past the sequence hold the next sequence's queries (or zeros
+      // past the batch); their results are never written.
+      const bool q_ok = __all_sync(0xffffffffu, mbar_wait(bar(B_Q_FULL), 0));
+      if (q_ok) {
+        const unsigned char* qrow = smem + S_RING + r * 128;
 #pragma unroll 1
         for (int c = 0; c < kChunksPerTile; ++c) {
           uint32_t v[32];
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            uint4 x = make_uint4(0, 0, 0, 0);
-            if (row_ok) x = c < 8 ? src[8 * c + q] : srp[q];
+            const uint4 x = *reinterpret_cast<const uint4*>(qrow + c * (kBM * 128) +
+                                                             ((q ^ (r & 7)) << 4));
             v[4 * q + 0] = x.x;
             v[4 * q + 1] = x.y;
             v[4 * q + 2] = x.z;
@@ -401,16 +435,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tmem_st32(t_lane + kTmemQ + 32 * c, v);
         }
         tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_Q_TMEM));
       }
+      fence_proxy_async_smem();  // the ring is refilled by TMA after this
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_Q_TMEM));
+      if (!row_barrier_and(q_ok)) failed = true;  // the four row warps agree
       const uint32_t msg_peer0 = map_peer(sbase + O_MSG, peer);
       const uint32_t pfull_peer0 = map_peer(bar(B_P_FULL), peer);
 
       const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
       float m_run = -INFINITY, l_run = 0.f;
-      for (int jj = 0; jj < nt; ++jj) {
+      for (int jj = 0; jj < nt && !failed; ++jj) {
         const int sb = jj & 1;
         const long long t0 = (long long)tile_of(jj) * kBN;
         bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_S_FULL + sb), (jj >> 1) & 1));
@@ -611,7 +647,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         umma_commit(bar(B_MMA_DONE));
         if (!mbar_wait(bar(B_MMA_DONE), 0)) failed = true;
       }
-    } else {
+    } else if (warp >= 2 && warp <= 5) {
       // ---------------- row warps: rescales, message slot recycling, output ---
       const int qd = warp & 3;
       const int r = qd * 32 + lane;
@@ -629,23 +665,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const unsigned char* msg = smem + O_MSG + mb * kMsgStride;
         const uint4 fl = *reinterpret_cast<const uint4*>(msg + kPBytes + kBM * 4);
         if (jj > 0 && (fl.x | fl.y | fl.z | fl.w)) {
+          // only the quadrants whose flag is set touch their O rows
+          const uint32_t mine = qd == 0 ? fl.x : qd == 1 ? fl.y : qd == 2 ? fl.z : fl.w;
           const float f = reinterpret_cast<const float*>(msg + kPBytes)[r];
           ok = __all_sync(0xffffffffu, mbar_wait(bar(B_PV_DONE + ((jj - 1) & 1)), ((jj - 1) >> 1) & 1));
           if (!row_barrier_and(ok)) {
             failed = true;
             break;
           }
-          tc_fence_after();
+          if (mine) {
+            tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < 16; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(t_lane + 32 * c, ov);
-            tmem_ld_wait();
+            for (int c = 0; c < 16; ++c) {
+              uint32_t ov[32];
+              tmem_ld32(t_lane + 32 * c, ov);
+              tmem_ld_wait();
 #pragma unroll
-            for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * f);
-            tmem_st32(t_lane + 32 * c, ov);
+              for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * f);
+              tmem_st32(t_lane + 32 * c, ov);
+            }
+            tmem_st_wait();
           }
-          tmem_st_wait();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(B_O_READY));
@@ -668,38 +708,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                                  ((nt - 1) >> 1) & 1)))
         failed = true;
       if (!failed) {
+        // Each row is staged in shared memory (the ring and message slots are
+        // idle once the last PV has completed) and written with one 1 KB bulk
+        // copy per pass: a warp's direct stores would touch 32 rows 2 KB apart.
         tc_fence_after();
         const float inv_l = reinterpret_cast<const float*>(smem + O_FIN)[r];
         const long long grow = row0 + r;
+        unsigned char* stage = smem + O_RING + r * kOutStride;
+        const uint32_t stage_s = sbase + O_RING + r * kOutStride;
+        const bool bf16_out = p.n_split == 1;
+        const int n_pass = bf16_out ? 1 : 2;  // 1 KB per pass: 512 bf16 or 256 fp32
 #pragma unroll 1
-        for (int c = 0; c < 16; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(t_lane + 32 * c, ov);
-          tmem_ld_wait();
-          if (!row_ok) continue;
-          if (p.n_split == 1) {
-            uint4* dst = reinterpret_cast<uint4*>(p.out + grow * kC + 32 * c);
+        for (int pass = 0; pass < n_pass; ++pass) {
+          if (pass > 0) bulk_wait_read0();  // the previous copy has read the stage
+#pragma unroll 1
+          for (int cc = 0; cc < (bf16_out ? 16 : 8); ++cc) {
+            const int c = pass * 8 + cc;  // 32-column group
+            uint32_t ov[32];
+            tmem_ld32(t_lane + 32 * c, ov);
+            tmem_ld_wait();
+            if (bf16_out) {
+              uint4* dst = reinterpret_cast<uint4*>(stage + cc * 64);
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              dst[q] = make_uint4(pack_bf16(__uint_as_float(ov[8 * q + 0]) * inv_l,
-                                            __uint_as_float(ov[8 * q + 1]) * inv_l),
-                                  pack_bf16(__uint_as_float(ov[8 * q + 2]) * inv_l,
-                                            __uint_as_float(ov[8 * q + 3]) * inv_l),
-                                  pack_bf16(__uint_as_float(ov[8 * q + 4]) * inv_l,
-                                            __uint_as_float(ov[8 * q + 5]) * inv_l),
-                                  pack_bf16(__uint_as_float(ov[8 * q + 6]) * inv_l,
-                                            __uint_as_float(ov[8 * q + 7]) * inv_l));
-          } else {
-            float4* dst = reinterpret_cast<float4*>(
-                p.part_o + ((long long)sp * total_rows + grow) * kC + 32 * c);
+              for (int q = 0; q < 4; ++q)
+                dst[q] = make_uint4(pack_bf16(__uint_as_float(ov[8 * q + 0]) * inv_l,
+                                              __uint_as_float(ov[8 * q + 1]) * inv_l),
+                                    pack_bf16(__uint_as_float(ov[8 * q + 2]) * inv_l,
+                                              __uint_as_float(ov[8 * q + 3]) * inv_l),
+                                    pack_bf16(__uint_as_float(ov[8 * q + 4]) * inv_l,
+                                              __uint_as_float(ov[8 * q + 5]) * inv_l),
+                                    pack_bf16(__uint_as_float(ov[8 * q + 6]) * inv_l,
+                                              __uint_as_float(ov[8 * q + 7]) * inv_l));
+            } else {
+              float4* dst = reinterpret_cast<float4*>(stage + cc * 128);
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              dst[q] = make_float4(__uint_as_float(ov[4 * q + 0]) * inv_l,
-                                   __uint_as_float(ov[4 * q + 1]) * inv_l,
-                                   __uint_as_float(ov[4 * q + 2]) * inv_l,
-                                   __uint_as_float(ov[4 * q + 3]) * inv_l);
+              for (int q = 0; q < 8; ++q)
+                dst[q] = make_float4(__uint_as_float(ov[4 * q + 0]) * inv_l,
+                                     __uint_as_float(ov[4 * q + 1]) * inv_l,
+                                     __uint_as_float(ov[4 * q + 2]) * inv_l,
+                                     __uint_as_float(ov[4 * q + 3]) * inv_l);
+            }
           }
+          fence_proxy_async_smem();
+          if (row_ok) {
+            void* gdst = bf16_out ? static_cast<void*>(p.out + grow * kC)
+                                  : static_cast<void*>(p.part_o +
+                                                       ((long long)sp * total_rows + grow) * kC +
+                                                       pass * 256);
+            bulk_s2g(gdst, stage_s, 1024);
+          }
+          bulk_commit();
         }
+        bulk_wait0();
       }
     }
   }
@@ -826,6 +886,30 @@ bool encode_kv_3d(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Q as {64 dims, rows, 8 chunks} (q_lat, row stride 1 KB) and {64 dims, rows}
+// (q_pe, row stride 128 B); a box of 128 rows lands as 128-row x 128-byte
+// swizzled chunks, the layout the row warps read back for TMEM.
+bool encode_q(CUtensorMap* ml, CUtensorMap* mp, const void* q_lat, const void* q_pe,
+              uint64_t rows) {
+  auto fn = encoder();
+  if (fn == nullptr) return false;
+  cuuint64_t dl[3] = {64, rows, (cuuint64_t)(kC / 64)};
+  cuuint64_t sl[2] = {(cuuint64_t)kC * 2, 128};
+  cuuint32_t bl[3] = {64, (cuuint32_t)kBM, (cuuint32_t)(kC / 64)};
+  cuuint32_t e3[3] = {1, 1, 1};
+  if (fn(ml, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q_lat), dl, sl, bl, e3,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  cuuint64_t dp[2] = {64, rows};
+  cuuint64_t sp[1] = {(cuuint64_t)kR * 2};
+  cuuint32_t bp[2] = {64, (cuuint32_t)kBM};
+  cuuint32_t e2[2] = {1, 1};
+  return fn(mp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q_pe), dp, sp, bp, e2,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 size_t verify_attn_bf16_workspace(const ddt_attn_dims& d) {
@@ -846,9 +930,10 @@ cudaError_t launch_verify_attn_bf16(const ddt_attn_dims& d, const void* q_lat, c
   if (d.kv_rows < 1 || rows > 0x7fffffffLL || d.kv_rows > 0x7fffffffLL)
     return cudaErrorInvalidValue;
   // the cache as {64 dims, rows, 9 chunks} with strides (row, 128 B)
-  CUtensorMap tm_s, tm_o;
+  CUtensorMap tm_s, tm_o, tm_ql, tm_qp;
   if (!encode_kv_3d(&tm_s, kv, (uint64_t)d.kv_rows, kChunksPerTile) ||
-      !encode_kv_3d(&tm_o, kv, (uint64_t)d.kv_rows, 8))
+      !encode_kv_3d(&tm_o, kv, (uint64_t)d.kv_rows, 8) ||
+      !encode_q(&tm_ql, &tm_qp, q_lat, q_pe, (uint64_t)rows))
     return cudaErrorInvalidValue;
 
   Params p;
@@ -871,7 +956,7 @@ cudaError_t launch_verify_attn_bf16(const ddt_attn_dims& d, const void* q_lat, c
   cudaError_t e = ensure_smem_limit(k_verify_attn_bf16, (int)kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
   k_verify_attn_bf16<<<(unsigned)(pl.units * 2), kThreads, kSmemBytes, stream>>>(
-      tm_s, tm_o, p);
+      tm_s, tm_o, tm_ql, tm_qp, p);
   e = cudaGetLastError();
   if (e != cudaSuccess || pl.n_split == 1) return e;
   k_combine<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(rows, pl.n_split, p.part_o,
