@@ -314,7 +314,9 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     split = DB.ddt_verify_attn_workspace_size(buf.attn) > 0
-    launches_per_step = 3 + (1 if split else 0)
+    # build + attention (fused for bf16 when the candidate table is small), split merge, accept
+    fused = w.dtype == "bf16" and min(w.D, w.budget) * min(w.K, w.budget) <= 1024
+    launches_per_step = (2 if fused else 3) + (1 if split else 0)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 

@@ -354,15 +354,19 @@ def ddt_step(topk_logp, topk_ids, root_tok, budget: int, V: int, q_lat, q_pe, kv
     argmax at every tree slot (it needs the tree's slot order)."""
     tree = tree_build(topk_logp, topk_ids, root_tok, budget, V)
     o = lse = None
+    attn_status = np.zeros(len(np.asarray(prefix_len)), np.int32)
     if attention:
-        o, lse = verify_attention(q_lat, q_pe, kv, block_table, prefix_len, tree["vis_bits"],
-                                  scale, page_size, rows=attn_rows)
+        o, lse, attn_status = verify_attention(q_lat, q_pe, kv, block_table, prefix_len,
+                                               tree["vis_bits"], scale, page_size,
+                                               rows=attn_rows, max_pages=max_pages,
+                                               with_status=True)
     target = np.asarray(target_argmax_fn(tree), np.int32)
     D = np.asarray(topk_logp).shape[1]
     acc = tree_accept(tree["tokens"], tree["parents"], target, D)
     new_kv, new_len, cst = cache_compact(kv, block_table, prefix_len, acc["accept_idx"],
                                          acc["accept_len"], page_size, max_pages)
-    status = tree["status"] | acc["status"] | cst
+    # a step's status is the union of its stages' statuses
+    status = tree["status"] | attn_status | acc["status"] | cst
     return dict(tree=tree, o=o, lse=lse, target=target, accept=acc, kv=new_kv,
                 new_len=new_len, status=status)
 

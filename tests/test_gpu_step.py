@@ -38,8 +38,8 @@ def kv_bits(x: np.ndarray, dtype: str) -> np.ndarray:
     return np.ascontiguousarray(x, np.float32).view(np.int32)
 
 
-def check_step(w, rows=None):
-    batch = WL.make_batch(w)
+def check_step(w, rows=None, batch=None):
+    batch = batch if batch is not None else WL.make_batch(w)
     lay = batch.layout
     ref = O.ddt_step(batch.topk_logp, batch.topk_ids, batch.root_tok, w.budget, w.V, batch.q_lat,
                      batch.q_pe, batch.kv, lay.block_table, batch.prefix_len, w.scale,
@@ -99,3 +99,46 @@ def test_step_sweep_points(q_len, B, L):
     w = WL.sweep_point(q_len, B, L)
     rows = [(0, 0), (B - 1, q_len - 1), (B // 2, q_len // 2)]
     check_step(w, rows=rows)
+
+
+# ---- the bf16 step builds the tree inside the attention kernel when the
+# candidate table is small; these cover that path's edges and the fallback
+
+def test_step_bf16_large_candidate_table_runs_build_and_attention_apart():
+    # min(D, budget) * min(K, budget) = 1600 candidates: over the fused limit
+    w = WL.CONFIGS["c2"].with_(D=40, K=40, V=4096, prefix=300)
+    check_step(w, rows=[(0, 0), (0, 33), (0, 64)])
+
+
+def test_step_fused_build_with_invalid_drafter_input():
+    w = WL.CONFIGS["c2"].with_(B=3, V=4096, prefix=(70, 300))
+    batch = WL.make_batch(w)
+    batch.topk_logp = batch.topk_logp.copy()
+    batch.topk_ids = batch.topk_ids.copy()
+    batch.topk_logp[1, 2, 3] = np.nan      # sequence 1: the root alone, ST_INPUT
+    batch.topk_ids[2, 0, 0] = w.V + 5      # sequence 2 likewise
+    ref = check_step(w, rows=[(0, 5), (1, 0), (2, 64)], batch=batch)
+    assert (ref["status"][1:] & O.ST_INPUT).all() and not ref["status"][0] & O.ST_INPUT
+
+
+def test_step_fused_build_when_a_sequence_cannot_be_attended():
+    # sequence 1 has no room for the tree (capacity error): no cluster attends
+    # it, yet its tree is still built and written
+    w = WL.CONFIGS["c2"].with_(B=3, budget=8, prefix=100, V=4096, page_size=64)
+    batch = WL.make_batch(w)
+    batch.prefix_len = batch.prefix_len.copy()
+    batch.prefix_len[1] = batch.layout.max_pages * batch.layout.page_size
+    ref = check_step(w, rows=[(0, 0), (1, 3), (2, 8)], batch=batch)
+    assert ref["status"][1] & O.ST_CAPACITY
+
+
+def test_step_fused_build_short_prefixes_every_tile_holds_tree_keys():
+    # prefixes under one key tile: every cluster waits for the tree at once
+    w = WL.CONFIGS["c2"].with_(B=4, V=4096, prefix=(0, 60))
+    check_step(w, rows=[(0, 0), (1, 64), (3, 17), (2, 40)])
+
+
+def test_step_fused_build_budget_zero_and_one():
+    for budget in (0, 1):
+        w = WL.CONFIGS["c2"].with_(B=2, V=4096, budget=budget, prefix=(64, 200))
+        check_step(w)

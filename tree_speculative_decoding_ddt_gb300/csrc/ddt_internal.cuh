@@ -50,13 +50,36 @@ cudaError_t launch_verify_attn_f32(const ddt_attn_dims& d, const float* q_lat, c
                                    const int32_t* prefix_len, const uint64_t* vis_bits, float* out,
                                    float* lse, int32_t* status, cudaStream_t stream);
 
-// B. verify attention, bf16 tcgen05 path.
+// A inside B: the draft tree of each sequence is built by a spare warp of the
+// bf16 verify-attention kernel while the prefix part of the attention runs
+// (the key tiles that hold tree keys come last in every walk). One cluster
+// per sequence writes the tree outputs and OR-s the build's status bits.
+struct TreeFuse {
+  int32_t D, K, budget, V;
+  const float* topk_logp;
+  const int32_t* topk_ids;
+  const int32_t* root_tok;
+  int32_t* tokens;
+  int32_t* parents;
+  int32_t* depths;
+  uint64_t* vis_bits;
+  uint8_t* vis;  // may be null
+  int32_t* first_child;
+  int32_t* next_sibling;
+  int32_t* n_nodes;
+};
+// Largest candidate table (min(D,budget) x min(K,budget)) the fused build stages.
+constexpr int kFuseMaxCand = 1024;
+
+// B. verify attention, bf16 tcgen05 path. With `fuse`, vis_bits is not read:
+// the kernel builds the tree itself and status must be zero on entry.
 size_t verify_attn_bf16_workspace(const ddt_attn_dims& d);
 cudaError_t launch_verify_attn_bf16(const ddt_attn_dims& d, const void* q_lat, const void* q_pe,
                                     const void* kv, const int32_t* block_table,
                                     const int32_t* prefix_len, const uint64_t* vis_bits,
                                     void* out, float* lse, int32_t* status, void* workspace,
-                                    size_t workspace_bytes, cudaStream_t stream);
+                                    size_t workspace_bytes, cudaStream_t stream,
+                                    const TreeFuse* fuse = nullptr);
 
 // Host checks of a verify-attention call (defined in ddt_api.cu).
 int check_verify_attn_args(const ddt_attn_dims* d, const void* q_lat, const void* q_pe,

@@ -40,12 +40,14 @@
 // several clusters (split-KV); partial results are merged by k_combine.
 #include <cuda_bf16.h>
 #include <math.h>
+#include <stddef.h>
 #include <stdio.h>
 
 #include <cudaTypedefs.h>
 
 #include "ddt_internal.cuh"
 #include "sm100_ptx.cuh"
+#include "tree_build_warp.cuh"
 
 namespace ddt {
 namespace {
@@ -75,12 +77,15 @@ constexpr uint32_t kOutStride = 1040;                   // staged output row: 1 
 constexpr uint32_t S_RING = 0;
 constexpr uint32_t S_STAGE = S_RING + kStages * kTileS;  // 2 outgoing messages
 constexpr uint32_t S_FIN = S_STAGE + 2 * kMsgStride;
-constexpr uint32_t S_END = S_FIN + 1024;
+constexpr uint32_t S_VIS = S_FIN + 1024;  // ancestor words of the fused build [kMaxQ][kMaxW]
+constexpr uint32_t S_END = S_VIS + kMaxQ * kMaxW * 8;
 // O-CTA shared memory
 constexpr uint32_t O_RING = 0;
 constexpr uint32_t O_MSG = O_RING + kStages * kTileO;  // 2 incoming messages
 constexpr uint32_t O_FIN = O_MSG + 2 * kMsgStride;
-constexpr uint32_t O_END = O_FIN + 1024;
+constexpr uint32_t O_BUILD = O_FIN + 1024;  // fused tree build: tb::Smem + staged candidates
+constexpr uint32_t kBuildBytes = (uint32_t)tb::smem_bytes(kFuseMaxCand, 1);
+constexpr uint32_t O_END = O_BUILD + ((kBuildBytes + 1023) & ~1023u);
 
 constexpr uint32_t OFF_BAR = (S_END > O_END ? S_END : O_END);
 constexpr uint32_t kSmemBytes = OFF_BAR + 1024 + 1024;  // barriers + alignment slack
@@ -89,6 +94,7 @@ static_assert(kMsgBytes <= kMsgStride && kMsgBytes % 16 == 0, "message size");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 static_assert(kQBytes <= kStages * kTileS, "the Q tile is staged in the S-CTA ring");
 static_assert(kBM * kOutStride <= O_FIN, "the output is staged in the O-CTA ring and messages");
+static_assert(offsetof(tb::Smem, anc) % 16 == 0, "ancestor words are bulk-copied");
 
 // mbarriers (indices into one array; each CTA uses its own subset)
 enum Bar {
@@ -110,7 +116,8 @@ enum Bar {
   B_TAIL_OK = B_FIN_FULL + 1,
   // both
   B_MMA_DONE = B_TAIL_OK + 1,
-  N_BARS = B_MMA_DONE + 1
+  B_TREE = B_MMA_DONE + 1,  // S-CTA: ancestor words of the fused build landed
+  N_BARS = B_TREE + 1
 };
 static_assert(N_BARS * 8 + 16 <= 1024, "barrier area");
 
@@ -137,6 +144,8 @@ struct Params {
   int32_t* status;
   float* part_o;
   float* part_lse;
+  int fuse;     // build the tree here (vis_bits unused)
+  TreeFuse tf;  // its inputs and outputs
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -217,6 +226,33 @@ __device__ void write_empty(const Params& p, int b, int rt, int sp, uint32_t ran
   }
 }
 
+// The draft tree of sequence b, built by the calling warp into `bsm`
+// (tb::Smem + staged candidates). Returns the node count; *bad as tb::build_warp.
+__device__ int fused_build(const TreeFuse& f, int b, unsigned char* bsm, bool* bad) {
+  const int De = min(f.D, f.budget), Ke = min(f.K, f.budget);
+  tb::Smem& S = *reinterpret_cast<tb::Smem*>(bsm);
+  double* s_logp = reinterpret_cast<double*>(bsm + sizeof(tb::Smem));
+  int32_t* s_ids = reinterpret_cast<int32_t*>(s_logp + De * Ke);
+  const float* lp = f.topk_logp + (size_t)b * f.D * f.K;
+  const int32_t* ip = f.topk_ids + (size_t)b * f.D * f.K;
+  const int32_t root = f.root_tok[b];
+  switch (tb::slots_for(f.budget + 1)) {
+    case 1: return tb::build_warp<1>(lp, ip, root, f.D, f.K, f.budget, f.V, De, Ke, S, s_logp, s_ids, bad);
+    case 2: return tb::build_warp<2>(lp, ip, root, f.D, f.K, f.budget, f.V, De, Ke, S, s_logp, s_ids, bad);
+    case 3: return tb::build_warp<3>(lp, ip, root, f.D, f.K, f.budget, f.V, De, Ke, S, s_logp, s_ids, bad);
+    default: return tb::build_warp<4>(lp, ip, root, f.D, f.K, f.budget, f.V, De, Ke, S, s_logp, s_ids, bad);
+  }
+}
+// Tree outputs of sequence b from the build in `bsm`; OR-s the build's status bits.
+__device__ void fused_write(const Params& p, int b, const unsigned char* bsm, int n, bool bad) {
+  const TreeFuse& f = p.tf;
+  const int32_t st = tb::write_warp(*reinterpret_cast<const tb::Smem*>(bsm), b, f.budget + 1, n,
+                                    bad, f.tokens, f.parents, f.depths,
+                                    reinterpret_cast<unsigned long long*>(f.vis_bits), f.vis,
+                                    f.first_child, f.next_sibling, f.n_nodes);
+  if ((threadIdx.x & 31) == 0 && st != 0) atomicOr(p.status + b, st);
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     k_verify_attn_bf16(const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_o,
                        const __grid_constant__ CUtensorMap tm_ql,
@@ -262,11 +298,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int tps = (n_tiles + p.n_split - 1) / p.n_split;
   const int j_begin = sp * tps;
   const int nt = code ? 0 : max(0, min(n_tiles, j_begin + tps) - j_begin);
+  // with a fused build, the unit holding the sequence tail of row tile 0
+  // writes the tree (unit 0 when the sequence cannot be attended)
+  const int sp_last = code ? 0 : (n_tiles - 1) / tps;
+  const bool designated = p.fuse && rt == 0 && sp == sp_last;
   if (nt == 0) {
     write_empty(p, b, rt, sp, rank);
     if (code && rt == 0 && sp == 0 && rank == 0 && tid == 0) atomicOr(p.status + b, code);
+    if (designated && rank == 1 && warp == 6) {
+      bool bad = false;
+      const int n = fused_build(p.tf, b, smem + O_BUILD, &bad);
+      fused_write(p, b, smem + O_BUILD, n, bad);
+    }
     return;  // both CTAs of the cluster take this branch together
   }
+  // Row tiles of a sequence walk its key tiles from staggered starting points
+  // (all clusters reading the same tile at once contend for the same L2
+  // lines). Only tiles that lie wholly in the prefix rotate; the tiles that
+  // hold tree keys come last, in order, so that the running max is taken
+  // over full prefix tiles before the sparse, masked tree tiles (a walk that
+  // starts on a tile with a handful of visible keys rescales O again and
+  // again), so that a tree built in this kernel is needed as late as
+  // possible, and so that the unit's last tile, which holds the sequence
+  // tail, stays last. The online softmax does not depend on the order.
+  const int n_pure = (int)(L / kBN);  // tiles with no tree key
+  const int nrot = max(0, min(j_begin + nt, n_pure) - j_begin);
+  // units with tree tiles build the tree themselves (the designated one has)
+  const bool builds = p.fuse && nt > nrot;
+  const uint32_t vis_bytes = (uint32_t)(p.Q * kMaxW * 8);
 
   // ---- setup ---------------------------------------------------------------
   if (tid == 0) {
@@ -283,6 +342,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_Q_TMEM), 4);
       mbar_init(bar(B_Q_FULL), 1);
       mbar_init(bar(B_MMA_DONE), 2);  // one commit per MMA issuer
+      if (builds) {
+        mbar_init(bar(B_TREE), 1);
+        mbar_expect_tx(bar(B_TREE), vis_bytes);
+      }
     } else {
       for (int s = 0; s < kStages; ++s) {
         mbar_init(bar(B_HALF_FULL + s), 1);
@@ -314,16 +377,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   bool failed = false;
   const long long row0 = (long long)b * QH + (long long)rt * kBM;
-  // Row tiles of a sequence walk its key tiles from staggered starting points
-  // (all clusters reading the same tile at once contend for the same L2
-  // lines). Only tiles that lie wholly in the prefix rotate; the tiles that
-  // hold tree keys come last, in order, so that the running max is taken
-  // over full prefix tiles before the sparse, masked tree tiles (a walk that
-  // starts on a tile with a handful of visible keys rescales O again and
-  // again), and the unit's last tile, which holds the sequence tail, stays
-  // last. The online softmax does not depend on the order.
-  const int n_pure = (int)(L / kBN);  // tiles with no tree key
-  const int nrot = max(0, min(j_begin + nt, n_pure) - j_begin);
   const int rot = nrot > 0 ? (int)(((long long)rt * nrot) / p.n_rt) : 0;
   auto tile_of = [&](int jj) -> int {
     return (jj < nrot) ? j_begin + (jj + rot) % nrot : j_begin + jj;
@@ -408,7 +461,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int qi = row_ok ? lr / p.H : 0;
       const int W = (p.Q + 63) >> 6;
       unsigned long long vis0 = 0ull, vis1 = 0ull;
-      if (row_ok) {
+      bool vis_ready = !p.fuse;  // a fused build delivers them before the first tree tile
+      if (!p.fuse && row_ok) {
         const unsigned long long* vb = p.vis_bits + ((size_t)b * p.Q + qi) * W;
         vis0 = vb[0];
         if (W > 1) vis1 = vb[1];
@@ -472,6 +526,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(bar(B_S_EMPTY + sb));
 
         // mask: keys past the prefix are visible only along the ancestor path
+        if (t0 + kBN > L && !vis_ready) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(B_TREE), 0));
+          if (!row_barrier_and(ok)) {
+            failed = true;
+            break;
+          }
+          if (row_ok) {
+            const unsigned long long* vw =
+                reinterpret_cast<const unsigned long long*>(smem + S_VIS) + qi * kMaxW;
+            vis0 = vw[0];
+            vis1 = vw[1];
+          }
+          vis_ready = true;
+        }
         if (t0 + kBN > L) {
 #pragma unroll
           for (int k = 0; k < 64; ++k) {
@@ -702,7 +770,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           mbar_arrive_cluster(pfree_peer0 + 8 * mb);
         }
       }
-      // ---- epilogue: O / l ------------------------------------------------------
+      // ---- epilogue: O / l ---------------------------------------------------
       if (!__all_sync(0xffffffffu, !failed && mbar_wait_cluster(bar(B_FIN_FULL), 0) &&
                                        mbar_wait(bar(B_PV_DONE + ((nt - 1) & 1)),
                                                  ((nt - 1) >> 1) & 1)))
@@ -761,9 +829,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         bulk_wait0();
       }
+    } else if (warp == 6) {
+      // ---------------- the fused tree build --------------------------------
+      if (builds) {
+        bool bad = false;
+        const int n = fused_build(p.tf, b, smem + O_BUILD, &bad);
+        // the S-CTA needs the ancestor words first; the outputs follow
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0)
+          bulk_copy_to_peer(map_peer(sbase + S_VIS, peer),
+                            sbase + O_BUILD + (uint32_t)offsetof(tb::Smem, anc), vis_bytes,
+                            map_peer(bar(B_TREE), peer));
+        if (designated) fused_write(p, b, smem + O_BUILD, n, bad);
+      }
     }
   }
 
+  // the ancestor words sent by the peer have landed before this CTA leaves
+  if (builds && rank == 0 && tid == 0 && !mbar_wait(bar(B_TREE), 0)) failed = true;
   if (failed) atomicOr(p.status + b, DDT_ST_TIMEOUT);
   __syncthreads();
   if (warp == 1) {
@@ -924,7 +1008,8 @@ cudaError_t launch_verify_attn_bf16(const ddt_attn_dims& d, const void* q_lat, c
                                     const void* kv, const int32_t* block_table,
                                     const int32_t* prefix_len, const uint64_t* vis_bits,
                                     void* out, float* lse, int32_t* status, void* workspace,
-                                    size_t workspace_bytes, cudaStream_t stream) {
+                                    size_t workspace_bytes, cudaStream_t stream,
+                                    const TreeFuse* fuse) {
   const Plan pl = make_plan(d);
   const long long rows = (long long)d.B * d.Q * d.H;
   if (d.kv_rows < 1 || rows > 0x7fffffffLL || d.kv_rows > 0x7fffffffLL)
@@ -948,6 +1033,8 @@ cudaError_t launch_verify_attn_bf16(const ddt_attn_dims& d, const void* q_lat, c
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse; p.status = status;
   p.part_o = nullptr; p.part_lse = nullptr;
+  p.fuse = fuse != nullptr ? 1 : 0;
+  p.tf = fuse != nullptr ? *fuse : TreeFuse{};
   if (pl.n_split > 1) {
     p.part_o = static_cast<float*>(workspace);
     p.part_lse = p.part_o + (size_t)pl.n_split * rows * kC;
