@@ -541,16 +541,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           vis_ready = true;
         }
         if (t0 + kBN > L) {
+          // visibility of the tile's 64 keys as one word: key k is slot t0 + k;
+          // slots below L are prefix, slot L + t is tree slot t (bit t of the
+          // row's ancestor words vis1:vis0), slots from n_keys on do not exist
+          const int np = (int)max(0ll, L - t0);           // prefix keys in the tile, < 64
+          const int off = (int)(t0 - L);                 // tree slot of key 0, in (-64, 128)
+          const int nk = (int)min(64ll, n_keys - t0);    // keys that exist, in (0, 64]
+          unsigned long long tm;
+          if (off < 0) tm = vis0 << (-off);
+          else if (off == 0) tm = vis0;
+          else if (off < 64) tm = (vis0 >> off) | (vis1 << (64 - off));
+          else tm = vis1 >> (off - 64);
+          const unsigned long long pm = (1ull << np) - 1ull;
+          const unsigned long long km = nk >= 64 ? ~0ull : (1ull << nk) - 1ull;
+          const unsigned long long m = (pm | tm) & km;
 #pragma unroll
-          for (int k = 0; k < 64; ++k) {
-            const long long slot = t0 + k;
-            bool vis = slot < L;
-            if (!vis && slot < n_keys) {
-              const int t = (int)(slot - L);
-              vis = ((t < 64 ? vis0 : vis1) >> (t & 63)) & 1ull;
-            }
-            if (!vis) x[k] = -INFINITY;
-          }
+          for (int k = 0; k < 64; ++k)
+            if (!((m >> k) & 1ull)) x[k] = -INFINITY;
         }
         float mx8[8];
 #pragma unroll
@@ -640,9 +647,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else {
     // ========================= O-CTA =========================
     if (warp == 0) {
+      int u = 0;
       if (lane == 0) {  // TMA: one 64 KB request (the c_kv part) per tile
         prefetch_tmap(&tm_o);
-        int u = 0;
         for (; u < nt; ++u) {
           const int slot = u % kStages;
           if (u >= kStages && !mbar_wait(bar(B_HALF_EMPTY + slot), ((u / kStages) - 1) & 1)) {
@@ -655,22 +662,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         for (int v = max(0, u - kStages); v < u; ++v)
           if (!mbar_wait(bar(B_HALF_FULL + v % kStages), (v / kStages) & 1)) failed = true;
-        // keys past the end of the sequence in the last tile: zero their values
-        // so that 0 * (whatever the page holds) cannot turn into NaN
-        if (!failed && u == nt) {
-          const long long t0 = (long long)(j_begin + nt - 1) * kBN;
-          if (t0 + kBN > n_keys) {
-            unsigned char* base = smem + O_RING + ((nt - 1) % kStages) * kTileO;
-            for (int rr = (int)(n_keys - t0); rr < kBN; ++rr)
-              for (int c = 0; c < 8; ++c) {
-                uint4* row = reinterpret_cast<uint4*>(base + c * kChunkBytes + (rr >> 3) * 1024 +
-                                                      (rr & 7) * 128);
-                for (int q = 0; q < 8; ++q) row[q] = make_uint4(0, 0, 0, 0);
-              }
+      }
+      // keys past the end of the sequence in the last tile: the warp zeroes
+      // their values so that 0 * (whatever the page holds) cannot turn into NaN
+      if (__shfl_sync(0xffffffffu, (!failed && u == nt) ? 1 : 0, 0)) {
+        const long long t0 = (long long)(j_begin + nt - 1) * kBN;
+        if (t0 + kBN > n_keys) {
+          unsigned char* base = smem + O_RING + ((nt - 1) % kStages) * kTileO;
+          const int r0 = (int)(n_keys - t0);
+          for (int e = lane; e < (kBN - r0) * 64; e += 32) {  // 16-byte units
+            const int rr = r0 + (e >> 6), c = (e >> 3) & 7, q = e & 7;
+            reinterpret_cast<uint4*>(base + c * kChunkBytes + (rr >> 3) * 1024 +
+                                     (rr & 7) * 128)[q] = make_uint4(0, 0, 0, 0);
           }
-          fence_proxy_async_smem();
-          mbar_arrive(bar(B_TAIL_OK));
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_TAIL_OK));
       }
     } else if (warp == 1) {
       if (lane == 0) {  // PV: A = P (K-major, from the S-CTA), B = V half (MN-major)
