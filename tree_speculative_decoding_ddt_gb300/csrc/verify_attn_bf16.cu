@@ -66,6 +66,7 @@ constexpr uint32_t kTileS = kChunksPerTile * kChunkBytes;  // S-CTA stage: 72 KB
 constexpr uint32_t kTileO = 8 * kChunkBytes;               // O-CTA stage: c_kv, 64 KB
 constexpr uint32_t kHalfBytes = 4 * kChunkBytes;           // 256 c_kv dims x 64 keys
 constexpr int kStages = 2;
+constexpr int kMsgSlots = 3;  // P messages in flight between the two CTAs
 constexpr uint32_t kPBytes = kBM * 128;                 // P tile: 128 rows x 64 keys bf16
 constexpr uint32_t kMsgBytes = kPBytes + kBM * 4 + 16;  // P | per-row factor | 4 warp flags
 constexpr uint32_t kMsgStride = 17408;                  // 1 KB aligned message slots
@@ -75,14 +76,14 @@ constexpr uint32_t kOutStride = 1040;                   // staged output row: 1 
 
 // S-CTA shared memory
 constexpr uint32_t S_RING = 0;
-constexpr uint32_t S_STAGE = S_RING + kStages * kTileS;  // 2 outgoing messages
-constexpr uint32_t S_FIN = S_STAGE + 2 * kMsgStride;
+constexpr uint32_t S_STAGE = S_RING + kStages * kTileS;  // outgoing messages
+constexpr uint32_t S_FIN = S_STAGE + kMsgSlots * kMsgStride;
 constexpr uint32_t S_VIS = S_FIN + 1024;  // ancestor words of the fused build [kMaxQ][kMaxW]
 constexpr uint32_t S_END = S_VIS + kMaxQ * kMaxW * 8;
 // O-CTA shared memory
 constexpr uint32_t O_RING = 0;
-constexpr uint32_t O_MSG = O_RING + kStages * kTileO;  // 2 incoming messages
-constexpr uint32_t O_FIN = O_MSG + 2 * kMsgStride;
+constexpr uint32_t O_MSG = O_RING + kStages * kTileO;  // incoming messages
+constexpr uint32_t O_FIN = O_MSG + kMsgSlots * kMsgStride;
 constexpr uint32_t O_BUILD = O_FIN + 1024;  // fused tree build: tb::Smem + staged candidates
 constexpr uint32_t kBuildBytes = (uint32_t)tb::smem_bytes(kFuseMaxCand, 1);
 constexpr uint32_t O_END = O_BUILD + ((kBuildBytes + 1023) & ~1023u);
@@ -107,12 +108,15 @@ enum Bar {
   B_Q_FULL = B_Q_TMEM + 1,  // Q tile landed in the ring (TMA)
   B_P_FREE = B_Q_FULL + 1,  // +message slot; arrived by the O-CTA
   // O-CTA
-  B_HALF_FULL = B_P_FREE + 2,            // +stage
+  B_HALF_FULL = B_P_FREE + kMsgSlots,    // +stage
   B_HALF_EMPTY = B_HALF_FULL + kStages,  // +stage
   B_P_FULL = B_HALF_EMPTY + kStages,     // +message slot; completed by the S-CTA's copy
-  B_O_READY = B_P_FULL + 2,
-  B_PV_DONE = B_O_READY + 1,  // +tile parity
-  B_FIN_FULL = B_PV_DONE + 2,
+  B_O_READY = B_P_FULL + kMsgSlots,
+  // +message slot: PV of the tile in that slot has completed (one barrier per
+  // slot: a barrier cannot complete another phase before the row warps have
+  // waited on this one, since its next tile needs the slot back)
+  B_PV_DONE = B_O_READY + 1,
+  B_FIN_FULL = B_PV_DONE + kMsgSlots,
   B_TAIL_OK = B_FIN_FULL + 1,
   // both
   B_MMA_DONE = B_TAIL_OK + 1,
@@ -337,8 +341,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int s = 0; s < 2; ++s) {
         mbar_init(bar(B_S_FULL + s), 1);
         mbar_init(bar(B_S_EMPTY + s), 4);
-        mbar_init(bar(B_P_FREE + s), 1);
       }
+      for (int s = 0; s < kMsgSlots; ++s) mbar_init(bar(B_P_FREE + s), 1);
       mbar_init(bar(B_Q_TMEM), 4);
       mbar_init(bar(B_Q_FULL), 1);
       mbar_init(bar(B_MMA_DONE), 2);  // one commit per MMA issuer
@@ -351,15 +355,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(bar(B_HALF_FULL + s), 1);
         mbar_init(bar(B_HALF_EMPTY + s), 1);
       }
-      for (int s = 0; s < 2; ++s) mbar_init(bar(B_P_FULL + s), 1);
+      for (int s = 0; s < kMsgSlots; ++s) {
+        mbar_init(bar(B_P_FULL + s), 1);
+        mbar_init(bar(B_PV_DONE + s), 1);
+      }
       mbar_init(bar(B_O_READY), 4);
-      mbar_init(bar(B_PV_DONE + 0), 1);
-      mbar_init(bar(B_PV_DONE + 1), 1);
       mbar_init(bar(B_FIN_FULL), 1);
       mbar_init(bar(B_TAIL_OK), 1);
-      // arm the incoming messages 0 and 1 and the final 1/l vector
-      mbar_expect_tx(bar(B_P_FULL + 0), kMsgBytes);
-      if (nt > 1) mbar_expect_tx(bar(B_P_FULL + 1), kMsgBytes);
+      // arm the first incoming messages and the final 1/l vector
+      for (int s = 0; s < kMsgSlots && s < nt; ++s) mbar_expect_tx(bar(B_P_FULL + s), kMsgBytes);
       mbar_expect_tx(bar(B_FIN_FULL), kFinBytes);
       mbar_init(bar(B_MMA_DONE), 1);
     }
@@ -500,14 +504,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
       const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
       float m_run = -INFINITY, l_run = 0.f;
+      // One named barrier per tile (before the copy of P): each warp's waits
+      // are bounded and their results are AND-ed there, so that all four
+      // leave together when one gives up.
+      int rj = rot;  // tile_of(jj) without a division
       for (int jj = 0; jj < nt && !failed; ++jj) {
         const int sb = jj & 1;
-        const long long t0 = (long long)tile_of(jj) * kBN;
+        const long long t0 = (long long)(jj < nrot ? j_begin + rj : j_begin + jj) * kBN;
+        if (jj < nrot && ++rj == nrot) rj = 0;
         bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_S_FULL + sb), (jj >> 1) & 1));
-        if (!row_barrier_and(ok)) {
-          failed = true;
-          break;
-        }
         tc_fence_after();
         float x[64];  // raw scores q.k (the scale is applied inside the exponent)
         {
@@ -527,11 +532,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
         // mask: keys past the prefix are visible only along the ancestor path
         if (t0 + kBN > L && !vis_ready) {
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(B_TREE), 0));
-          if (!row_barrier_and(ok)) {
-            failed = true;
-            break;
-          }
+          ok = ok && __all_sync(0xffffffffu, mbar_wait(bar(B_TREE), 0));
           if (row_ok) {
             const unsigned long long* vw =
                 reinterpret_cast<const unsigned long long*>(smem + S_VIS) + qi * kMaxW;
@@ -595,15 +596,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const float2 a = fadd2(a01, a23);
         l_run += a.x + a.y;
 
-        // outgoing message jj % 2 (and the peer's slot) are free once the peer
-        // has finished PV of tile jj-2
-        const int mb = jj & 1;
-        ok = jj < 2 ||
-             __all_sync(0xffffffffu, mbar_wait_cluster(bar(B_P_FREE + mb), ((jj >> 1) - 1) & 1));
-        if (!row_barrier_and(ok)) {
-          failed = true;
-          break;
-        }
+        // outgoing message slot jj % kMsgSlots (and the peer's) is free once
+        // the peer has finished PV of the tile that used it before
+        const int mb = jj % kMsgSlots;
+        ok = ok && (jj < kMsgSlots ||
+                    __all_sync(0xffffffffu, mbar_wait_cluster(bar(B_P_FREE + mb),
+                                                              ((jj / kMsgSlots) - 1) & 1)));
         unsigned char* msg = smem + S_STAGE + mb * kMsgStride;
         const uint32_t msg_s = sbase + S_STAGE + mb * kMsgStride;
         const uint32_t p_row = msg_s + (r >> 3) * 1024 + (r & 7) * 128;
@@ -618,7 +616,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const bool any_rescale = __any_sync(0xffffffffu, rescale);
         if (lane == 0) reinterpret_cast<uint32_t*>(msg + kPBytes + kBM * 4)[qd] = any_rescale;
         fence_proxy_async_smem();
-        row_barrier();
+        if (!row_barrier_and(ok)) {
+          failed = true;
+          break;
+        }
         if (tid == 64)
           bulk_copy_to_peer(msg_peer0 + mb * kMsgStride, msg_s, kMsgBytes, pfull_peer0 + 8 * mb);
       }
@@ -684,8 +685,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) {  // PV: A = P (K-major, from the S-CTA), B = V half (MN-major)
         int n_flag = 0;
         for (int jj = 0; jj < nt && !failed; ++jj) {
-          const int mb = jj & 1;
-          if (!mbar_wait_cluster(bar(B_P_FULL + mb), (jj >> 1) & 1)) {
+          const int mb = jj % kMsgSlots;
+          if (!mbar_wait_cluster(bar(B_P_FULL + mb), (jj / kMsgSlots) & 1)) {
             failed = true;
             break;
           }
@@ -717,7 +718,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             umma_bf16(tmem + 256, ad,
                       smem_desc(h1 + kk * 2048, kChunkBytes, 1024, kSwizzle128B), kIdescPV, acc);
           }
-          umma_commit(bar(B_PV_DONE + (jj & 1)));
+          umma_commit(bar(B_PV_DONE + mb));
           umma_commit(bar(B_HALF_EMPTY + slot));
         }
         umma_commit(bar(B_MMA_DONE));
@@ -732,8 +733,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const bool row_ok = lr < QH;
       const uint32_t pfree_peer0 = map_peer(bar(B_P_FREE), peer);
       for (int jj = 0; jj < nt; ++jj) {
-        const int mb = jj & 1;
-        bool ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar(B_P_FULL + mb), (jj >> 1) & 1));
+        const int mb = jj % kMsgSlots;
+        bool ok = __all_sync(0xffffffffu,
+                             mbar_wait_cluster(bar(B_P_FULL + mb), (jj / kMsgSlots) & 1));
         if (!row_barrier_and(ok)) {
           failed = true;
           break;
@@ -744,7 +746,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // only the quadrants whose flag is set touch their O rows
           const uint32_t mine = qd == 0 ? fl.x : qd == 1 ? fl.y : qd == 2 ? fl.z : fl.w;
           const float f = reinterpret_cast<const float*>(msg + kPBytes)[r];
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(B_PV_DONE + ((jj - 1) & 1)), ((jj - 1) >> 1) & 1));
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(B_PV_DONE + (jj - 1) % kMsgSlots),
+                                                 ((jj - 1) / kMsgSlots) & 1));
           if (!row_barrier_and(ok)) {
             failed = true;
             break;
@@ -768,20 +771,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         // slot mb is free once PV of tile jj has completed; all row warps move
         // on together so that no warp can fall a message behind
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(B_PV_DONE + mb), (jj >> 1) & 1));
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(B_PV_DONE + mb), (jj / kMsgSlots) & 1));
         if (!row_barrier_and(ok)) {
           failed = true;
           break;
         }
         if (tid == 64) {
-          if (jj + 2 < nt) mbar_expect_tx(bar(B_P_FULL + mb), kMsgBytes);
+          if (jj + kMsgSlots < nt) mbar_expect_tx(bar(B_P_FULL + mb), kMsgBytes);
           mbar_arrive_cluster(pfree_peer0 + 8 * mb);
         }
       }
       // ---- epilogue: O / l ---------------------------------------------------
       if (!__all_sync(0xffffffffu, !failed && mbar_wait_cluster(bar(B_FIN_FULL), 0) &&
-                                       mbar_wait(bar(B_PV_DONE + ((nt - 1) & 1)),
-                                                 ((nt - 1) >> 1) & 1)))
+                                       mbar_wait(bar(B_PV_DONE + (nt - 1) % kMsgSlots),
+                                                 ((nt - 1) / kMsgSlots) & 1)))
         failed = true;
       if (!failed) {
         // Each row is staged in shared memory (the ring and message slots are
