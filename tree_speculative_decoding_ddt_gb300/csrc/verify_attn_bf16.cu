@@ -66,7 +66,7 @@ constexpr uint32_t kTileS = kChunksPerTile * kChunkBytes;  // S-CTA stage: 72 KB
 constexpr uint32_t kTileO = 8 * kChunkBytes;               // O-CTA stage: c_kv, 64 KB
 constexpr uint32_t kHalfBytes = 4 * kChunkBytes;           // 256 c_kv dims x 64 keys
 constexpr int kStages = 2;
-constexpr int kMsgSlots = 3;  // P messages in flight between the two CTAs
+constexpr int kMsgSlots = 4;  // P messages in flight between the two CTAs
 constexpr uint32_t kPBytes = kBM * 128;                 // P tile: 128 rows x 64 keys bf16
 constexpr uint32_t kMsgBytes = kPBytes + kBM * 4 + 16;  // P | per-row factor | 4 warp flags
 constexpr uint32_t kMsgStride = 17408;                  // 1 KB aligned message slots
