@@ -88,7 +88,10 @@ constexpr uint32_t O_BUILD = O_FIN + 1024;  // fused tree build: tb::Smem + stag
 constexpr uint32_t kBuildBytes = (uint32_t)tb::smem_bytes(kFuseMaxCand, 1);
 constexpr uint32_t O_END = O_BUILD + ((kBuildBytes + 1023) & ~1023u);
 
-constexpr uint32_t OFF_BAR = (S_END > O_END ? S_END : O_END);
+// both CTAs: the sequence's block-table row, read once by the page check
+constexpr int kBtMax = 1024;  // pages staged (longer rows are read from global memory)
+constexpr uint32_t OFF_BT = (S_END > O_END ? S_END : O_END);
+constexpr uint32_t OFF_BAR = OFF_BT + kBtMax * 4;
 constexpr uint32_t kSmemBytes = OFF_BAR + 1024 + 1024;  // barriers + alignment slack
 static_assert(S_STAGE % 1024 == 0 && O_MSG % 1024 == 0 && kMsgStride % 1024 == 0, "alignment");
 static_assert(kMsgBytes <= kMsgStride && kMsgBytes % 16 == 0, "message size");
@@ -146,7 +149,7 @@ struct Params {
   __nv_bfloat16* out;
   float* lse;
   int32_t* status;
-  float* part_o;
+  __nv_bfloat16* part_o;  // split-KV partial outputs (normalised by their own l)
   float* part_lse;
   int fuse;     // build the tree here (vis_bits unused)
   TreeFuse tf;  // its inputs and outputs
@@ -216,9 +219,8 @@ __device__ void write_empty(const Params& p, int b, int rt, int sp, uint32_t ran
       if (p.n_split == 1) {
         reinterpret_cast<uint4*>(p.out + grow * kC)[c] = make_uint4(0, 0, 0, 0);
       } else {
-        float4* dst = reinterpret_cast<float4*>(p.part_o + ((long long)sp * total + grow) * kC);
-        dst[2 * c] = make_float4(0.f, 0.f, 0.f, 0.f);
-        dst[2 * c + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        reinterpret_cast<uint4*>(p.part_o + ((long long)sp * total + grow) * kC)[c] =
+            make_uint4(0, 0, 0, 0);
       }
     } else if (c == 0) {
       if (p.n_split == 1) {
@@ -282,6 +284,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int QH = p.Q * p.H;
   const long long total_rows = (long long)p.B * QH;
   const int32_t* bt = p.block_table + (size_t)b * p.max_pages;
+  const long long row0 = (long long)b * QH + (long long)rt * kBM;
+
+  // Q depends on no check: the S-CTA starts its load before anything else
+  // (the checks below are dependent global reads), into the ring, which K
+  // takes over once Q is in TMEM. A unit that exits early waits for it.
+  if (rank == 0 && tid == 0) {
+    mbar_init(bar(B_Q_FULL), 1);
+    fence_mbar_init();
+    mbar_expect_tx(bar(B_Q_FULL), kQBytes);
+    tma_load_3d(sbase + S_RING, &tm_ql, 0, (int)row0, 0, bar(B_Q_FULL));
+    tma_load_2d(sbase + S_RING + 8 * kBM * 128, &tm_qp, 0, (int)row0, bar(B_Q_FULL));
+  }
 
   // ---- capacity and page checks: identical decision in both CTAs ---------
   const long long L = p.prefix_len[b];
@@ -292,8 +306,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const long long n_pages = (n_keys + p.page_size - 1) / p.page_size;
     const long long kv_pages = p.kv_rows / p.page_size;
     bool badp = false;
+    int32_t* s_bt = reinterpret_cast<int32_t*>(smem + OFF_BT);
     for (long long q = tid; q < n_pages; q += kThreads) {
-      const long long pg = bt[q];
+      const int32_t pg = bt[q];
+      if (q < kBtMax) s_bt[q] = pg;
       if (pg < 0 || pg >= kv_pages) badp = true;
     }
     if (__syncthreads_or(badp)) code = DDT_ST_RANGE;
@@ -307,6 +323,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int sp_last = code ? 0 : (n_tiles - 1) / tps;
   const bool designated = p.fuse && rt == 0 && sp == sp_last;
   if (nt == 0) {
+    if (rank == 0 && tid == 0) mbar_wait(bar(B_Q_FULL), 0);  // nothing lands after exit
     write_empty(p, b, rt, sp, rank);
     if (code && rt == 0 && sp == 0 && rank == 0 && tid == 0) atomicOr(p.status + b, code);
     if (designated && rank == 1 && warp == 6) {
@@ -344,7 +361,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       for (int s = 0; s < kMsgSlots; ++s) mbar_init(bar(B_P_FREE + s), 1);
       mbar_init(bar(B_Q_TMEM), 4);
-      mbar_init(bar(B_Q_FULL), 1);
       mbar_init(bar(B_MMA_DONE), 2);  // one commit per MMA issuer
       if (builds) {
         mbar_init(bar(B_TREE), 1);
@@ -380,14 +396,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();  // the peer's barriers are initialised before any remote operation
 
   bool failed = false;
-  const long long row0 = (long long)b * QH + (long long)rt * kBM;
   const int rot = nrot > 0 ? (int)(((long long)rt * nrot) / p.n_rt) : 0;
   auto tile_of = [&](int jj) -> int {
     return (jj < nrot) ? j_begin + (jj + rot) % nrot : j_begin + jj;
   };
   auto krow_of = [&](int jj) -> long long {
     const long long t0 = (long long)tile_of(jj) * kBN;
-    return (long long)bt[t0 / p.page_size] * p.page_size + t0 % p.page_size;
+    const long long pi = t0 / p.page_size;
+    const int32_t pg = pi < kBtMax ? reinterpret_cast<const int32_t*>(smem + OFF_BT)[pi] : bt[pi];
+    return (long long)pg * p.page_size + t0 % p.page_size;
   };
 
   if (rank == 0) {
@@ -395,11 +412,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 0) {
       if (lane == 0) {
         prefetch_tmap(&tm_s);
-        // Q (128 rows: 8 chunks of c_kv dims, then the rope part) lands in the
-        // ring first; the row warps move it to TMEM, then the ring takes K
-        mbar_expect_tx(bar(B_Q_FULL), kQBytes);
-        tma_load_3d(sbase + S_RING, &tm_ql, 0, (int)row0, 0, bar(B_Q_FULL));
-        tma_load_2d(sbase + S_RING + 8 * kBM * 128, &tm_qp, 0, (int)row0, bar(B_Q_FULL));
         int u = 0;
         // K may overwrite the ring once Q is in TMEM; the Q copy has always
         // landed before anything else is issued (or the CTA leaves)
@@ -787,57 +799,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                                  ((nt - 1) / kMsgSlots) & 1)))
         failed = true;
       if (!failed) {
-        // Each row is staged in shared memory (the ring and message slots are
-        // idle once the last PV has completed) and written with one 1 KB bulk
-        // copy per pass: a warp's direct stores would touch 32 rows 2 KB apart.
+        // Each row (512 bf16: the output, or this unit's split-KV partial) is
+        // staged in shared memory (the ring and message slots are idle once the
+        // last PV has completed) and written with one 1 KB bulk copy: a warp's
+        // direct stores would touch 32 rows 1 KB apart.
         tc_fence_after();
         const float inv_l = reinterpret_cast<const float*>(smem + O_FIN)[r];
         const long long grow = row0 + r;
         unsigned char* stage = smem + O_RING + r * kOutStride;
         const uint32_t stage_s = sbase + O_RING + r * kOutStride;
-        const bool bf16_out = p.n_split == 1;
-        const int n_pass = bf16_out ? 1 : 2;  // 1 KB per pass: 512 bf16 or 256 fp32
 #pragma unroll 1
-        for (int pass = 0; pass < n_pass; ++pass) {
-          if (pass > 0) bulk_wait_read0();  // the previous copy has read the stage
-#pragma unroll 1
-          for (int cc = 0; cc < (bf16_out ? 16 : 8); ++cc) {
-            const int c = pass * 8 + cc;  // 32-column group
-            uint32_t ov[32];
-            tmem_ld32(t_lane + 32 * c, ov);
-            tmem_ld_wait();
-            if (bf16_out) {
-              uint4* dst = reinterpret_cast<uint4*>(stage + cc * 64);
+        for (int c = 0; c < 16; c += 2) {  // two 32-column groups per wait
+          uint32_t ov[2][32];
+          tmem_ld32(t_lane + 32 * c, ov[0]);
+          tmem_ld32(t_lane + 32 * (c + 1), ov[1]);
+          tmem_ld_wait();
 #pragma unroll
-              for (int q = 0; q < 4; ++q)
-                dst[q] = make_uint4(pack_bf16(__uint_as_float(ov[8 * q + 0]) * inv_l,
-                                              __uint_as_float(ov[8 * q + 1]) * inv_l),
-                                    pack_bf16(__uint_as_float(ov[8 * q + 2]) * inv_l,
-                                              __uint_as_float(ov[8 * q + 3]) * inv_l),
-                                    pack_bf16(__uint_as_float(ov[8 * q + 4]) * inv_l,
-                                              __uint_as_float(ov[8 * q + 5]) * inv_l),
-                                    pack_bf16(__uint_as_float(ov[8 * q + 6]) * inv_l,
-                                              __uint_as_float(ov[8 * q + 7]) * inv_l));
-            } else {
-              float4* dst = reinterpret_cast<float4*>(stage + cc * 128);
+          for (int h = 0; h < 2; ++h) {
+            uint4* dst = reinterpret_cast<uint4*>(stage + (c + h) * 64);
 #pragma unroll
-              for (int q = 0; q < 8; ++q)
-                dst[q] = make_float4(__uint_as_float(ov[4 * q + 0]) * inv_l,
-                                     __uint_as_float(ov[4 * q + 1]) * inv_l,
-                                     __uint_as_float(ov[4 * q + 2]) * inv_l,
-                                     __uint_as_float(ov[4 * q + 3]) * inv_l);
-            }
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(pack_bf16(__uint_as_float(ov[h][8 * q + 0]) * inv_l,
+                                            __uint_as_float(ov[h][8 * q + 1]) * inv_l),
+                                  pack_bf16(__uint_as_float(ov[h][8 * q + 2]) * inv_l,
+                                            __uint_as_float(ov[h][8 * q + 3]) * inv_l),
+                                  pack_bf16(__uint_as_float(ov[h][8 * q + 4]) * inv_l,
+                                            __uint_as_float(ov[h][8 * q + 5]) * inv_l),
+                                  pack_bf16(__uint_as_float(ov[h][8 * q + 6]) * inv_l,
+                                            __uint_as_float(ov[h][8 * q + 7]) * inv_l));
           }
-          fence_proxy_async_smem();
-          if (row_ok) {
-            void* gdst = bf16_out ? static_cast<void*>(p.out + grow * kC)
-                                  : static_cast<void*>(p.part_o +
-                                                       ((long long)sp * total_rows + grow) * kC +
-                                                       pass * 256);
-            bulk_s2g(gdst, stage_s, 1024);
-          }
-          bulk_commit();
         }
+        fence_proxy_async_smem();
+        if (row_ok)
+          bulk_s2g(p.n_split == 1 ? p.out + grow * kC
+                                  : p.part_o + ((long long)sp * total_rows + grow) * kC,
+                   stage_s, 1024);
+        bulk_commit();
         bulk_wait0();
       }
     } else if (warp == 6) {
@@ -870,8 +867,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 // Merge of the split-KV partials: o = sum_s w_s o_s / sum_s w_s with
 // w_s = exp(lse_s - max lse); one warp per query row, 16 columns per lane.
+// The partials are bf16 (each already normalised by its own sum), which
+// halves their round trip through memory; the merge runs in fp32.
 __global__ void __launch_bounds__(256) k_combine(long long total_rows, int n_split,
-                                                 const float* __restrict__ part_o,
+                                                 const __nv_bfloat16* __restrict__ part_o,
                                                  const float* __restrict__ part_lse,
                                                  __nv_bfloat16* __restrict__ out,
                                                  float* __restrict__ lse_out) {
@@ -890,16 +889,19 @@ __global__ void __launch_bounds__(256) k_combine(long long total_rows, int n_spl
       if (ls == -INFINITY) continue;
       const float w = expf(ls - m);
       wsum += w;
-      const float4* src =
-          reinterpret_cast<const float4*>(part_o + ((long long)s * total_rows + row) * kC) +
-          lane * 4;
+      const uint4* src =
+          reinterpret_cast<const uint4*>(part_o + ((long long)s * total_rows + row) * kC) +
+          lane * 2;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 v = src[q];
-        acc[4 * q + 0] = fmaf(w, v.x, acc[4 * q + 0]);
-        acc[4 * q + 1] = fmaf(w, v.y, acc[4 * q + 1]);
-        acc[4 * q + 2] = fmaf(w, v.z, acc[4 * q + 2]);
-        acc[4 * q + 3] = fmaf(w, v.w, acc[4 * q + 3]);
+      for (int q = 0; q < 2; ++q) {
+        const uint4 v = src[q];
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[e]));
+          acc[8 * q + 2 * e] = fmaf(w, f.x, acc[8 * q + 2 * e]);
+          acc[8 * q + 2 * e + 1] = fmaf(w, f.y, acc[8 * q + 2 * e + 1]);
+        }
       }
     }
   }
@@ -1011,7 +1013,7 @@ size_t verify_attn_bf16_workspace(const ddt_attn_dims& d) {
   const Plan pl = make_plan(d);
   if (pl.n_split <= 1) return 0;
   const size_t rows = (size_t)d.B * d.Q * d.H;
-  const size_t bytes = (size_t)pl.n_split * rows * (kC * sizeof(float) + sizeof(float));
+  const size_t bytes = (size_t)pl.n_split * rows * (kC * sizeof(__nv_bfloat16) + sizeof(float));
   return (bytes + 255) & ~size_t(255);
 }
 
@@ -1047,8 +1049,8 @@ cudaError_t launch_verify_attn_bf16(const ddt_attn_dims& d, const void* q_lat, c
   p.fuse = fuse != nullptr ? 1 : 0;
   p.tf = fuse != nullptr ? *fuse : TreeFuse{};
   if (pl.n_split > 1) {
-    p.part_o = static_cast<float*>(workspace);
-    p.part_lse = p.part_o + (size_t)pl.n_split * rows * kC;
+    p.part_o = static_cast<__nv_bfloat16*>(workspace);
+    p.part_lse = reinterpret_cast<float*>(p.part_o + (size_t)pl.n_split * rows * kC);
   }
   static int smem_set[64] = {};
   cudaError_t e = ensure_smem_limit(k_verify_attn_bf16, (int)kSmemBytes, smem_set);
