@@ -315,7 +315,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (__syncthreads_or(badp)) code = DDT_ST_RANGE;
   }
   const int n_tiles = (int)((n_keys + kBN - 1) / kBN);
-  const int tps = (n_tiles + p.n_split - 1) / p.n_split;
+  // the last unit of a split sequence also walks the tree tiles (and builds
+  // the tree): the earlier units take the extra tile when the range divides
+  const int tps = p.n_split > 1 ? (n_tiles + p.n_split) / p.n_split : n_tiles;
   const int j_begin = sp * tps;
   const int nt = code ? 0 : max(0, min(n_tiles, j_begin + tps) - j_begin);
   // with a fused build, the unit holding the sequence tail of row tile 0
