@@ -87,10 +87,12 @@ def measured_peaks():
 # k_verify_attn_bf16 launch, from ncu captures of the kernel built from the
 # source whose sha256 is given; reported as null once that source changes.
 MEASURED_TRAFFIC = {
-    "c2_max_budget": ("274bc41f00b6ce50dbd03f0af2f36b02f9d0f3fd8f982357e6c07fbfc6ad82ae",
-                      9772544),
-    "c4_deep_long": ("274bc41f00b6ce50dbd03f0af2f36b02f9d0f3fd8f982357e6c07fbfc6ad82ae",
-                     556023808 + 116403712),
+    "c2_max_budget": ("ef00f2f1daac8551449d88589bbf9c567da818205732f9511a776cf3981e3cdf",
+                      9833728),
+    "c3_batched_paged": ("ef00f2f1daac8551449d88589bbf9c567da818205732f9511a776cf3981e3cdf",
+                         502738688 + 61799680),
+    "c4_deep_long": ("ef00f2f1daac8551449d88589bbf9c567da818205732f9511a776cf3981e3cdf",
+                     547618048 + 60359424),
 }
 
 
