@@ -131,6 +131,14 @@ int ddt_tree_build(const ddt_tree_dims* dims, const float* topk_logp, const int3
 /* Bytes of scratch ddt_verify_attn needs for these dims (0 = none). */
 size_t ddt_verify_attn_workspace_size(const ddt_attn_dims* dims);
 
+/* Query rows per tile (128 or 256) the DDT_BF16 verify attention uses for
+ * these dims on the current device: 256-row tiles run on paired SMs (four-CTA
+ * clusters) and are taken when padding a sequence's Q*H rows to a multiple of
+ * 256 costs at most 1/12 of them; the environment variable
+ * DDT_VERIFY_ATTN_ROWS (128 or 256) overrides the choice. Informational (no
+ * counterpart on the source pages); 0 for invalid or DDT_F32 dims. */
+int ddt_verify_attn_rows_per_tile(const ddt_attn_dims* dims);
+
 /* B. Tree-verify MLA-absorb attention.
  * "The Checkpoint: Committing a Working Native DDTree Engine", section "The
  * Message" (attention via the custom verify_attn in absorb form; KV-cache

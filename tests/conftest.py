@@ -18,3 +18,12 @@ def lib():
     """The loaded C-ABI library (built in-tree by the package's build step)."""
     from tree_speculative_decoding_ddt_gb300 import _binding
     return _binding.load()
+
+
+@pytest.fixture(params=["128", "256"])
+def attn_rows(request, monkeypatch):
+    """Row-tile height of the bf16 verify attention: every case using this
+    fixture runs on both kernels (two-CTA 128-row tiles and four-CTA 256-row
+    tiles on paired SMs), forced through DDT_VERIFY_ATTN_ROWS."""
+    monkeypatch.setenv("DDT_VERIFY_ATTN_ROWS", request.param)
+    return int(request.param)

@@ -73,18 +73,18 @@ def test_f32_k2_dims_q_len_1_is_decode():
 
 @pytest.mark.parametrize("L", [0, 1, 63, 64, 65, 700])
 @pytest.mark.parametrize("budget", [0, 8, 16, 64])
-def test_bf16_ragged_prefixes(L, budget):
+def test_bf16_ragged_prefixes(L, budget, attn_rows):
     w = WL.CONFIGS["c2"].with_(B=2, budget=budget, prefix=L, V=4096)
     run_case(w)
 
 
 @pytest.mark.parametrize("H", [16, 128])
-def test_bf16_other_head_counts(H):
+def test_bf16_other_head_counts(H, attn_rows):
     w = WL.CONFIGS["c2"].with_(B=2, H=H, budget=8, prefix=300, V=4096)
     run_case(w)
 
 
-def test_bf16_paged_variable_lengths_forced_splits():
+def test_bf16_paged_variable_lengths_forced_splits(attn_rows):
     w = WL.CONFIGS["c3"].with_(B=5, V=4096, prefix=(0, 1500))
     batch = WL.make_batch(w)
     run_case(w, batch)                      # the planner's own split
@@ -92,11 +92,11 @@ def test_bf16_paged_variable_lengths_forced_splits():
     run_case(w, batch, max_len=w.Q)         # no split at all
 
 
-def test_bf16_max_budget_workload_all_rows():
+def test_bf16_max_budget_workload_all_rows(attn_rows):
     run_case(WL.CONFIGS["c2"])
 
 
-def test_bf16_batched_paged_workload_sampled_rows():
+def test_bf16_batched_paged_workload_sampled_rows(attn_rows):
     w = WL.CONFIGS["c3"]
     g = np.random.default_rng(0)
     rows = [(int(b), int(i)) for b, i in zip(g.integers(0, w.B, 24), g.integers(0, w.Q, 24))]
@@ -104,14 +104,14 @@ def test_bf16_batched_paged_workload_sampled_rows():
     run_case(w, rows=rows)
 
 
-def test_bf16_deep_long_workload_sampled_rows():
+def test_bf16_deep_long_workload_sampled_rows(attn_rows):
     w = WL.CONFIGS["c4"]
     rows = [(0, 0), (1, 15), (3, 40), (7, 64), (5, 7)]
     run_case(w, rows=rows)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_capacity_and_page_errors(dtype):
+def test_capacity_and_page_errors(dtype, attn_rows):
     base = WL.CONFIGS["c2"].with_(B=3, budget=8, prefix=100, V=4096, dtype=dtype,
                                   page_size=64)
     batch = WL.make_batch(base)

@@ -76,18 +76,18 @@ def test_step_tiny_f32():
     check_step(WL.CONFIGS["c1"])
 
 
-def test_step_max_budget():
+def test_step_max_budget(attn_rows):
     check_step(WL.CONFIGS["c2"])
 
 
-def test_step_batched_paged():
+def test_step_batched_paged(attn_rows):
     g = np.random.default_rng(1)
     w = WL.CONFIGS["c3"]
     rows = [(int(b), int(i)) for b, i in zip(g.integers(0, w.B, 16), g.integers(0, w.Q, 16))]
     check_step(w, rows=rows)
 
 
-def test_step_deep_long_accepts_15_and_compacts():
+def test_step_deep_long_accepts_15_and_compacts(attn_rows):
     w = WL.CONFIGS["c4"]
     ref = check_step(w, rows=[(0, 0), (2, 15), (7, 64)])
     assert (ref["accept"]["accept_len"] == 15).all()
@@ -95,7 +95,7 @@ def test_step_deep_long_accepts_15_and_compacts():
 
 @pytest.mark.parametrize("q_len,B,L", [(1, 8, 1024), (9, 64, 1024), (33, 1, 8192),
                                        (65, 8, 8192), (17, 1, 131072), (1, 8, 131072)])
-def test_step_sweep_points(q_len, B, L):
+def test_step_sweep_points(q_len, B, L, attn_rows):
     w = WL.sweep_point(q_len, B, L)
     rows = [(0, 0), (B - 1, q_len - 1), (B // 2, q_len // 2)]
     check_step(w, rows=rows)
@@ -104,13 +104,13 @@ def test_step_sweep_points(q_len, B, L):
 # ---- the bf16 step builds the tree inside the attention kernel when the
 # candidate table is small; these cover that path's edges and the fallback
 
-def test_step_bf16_large_candidate_table_runs_build_and_attention_apart():
+def test_step_bf16_large_candidate_table_runs_build_and_attention_apart(attn_rows):
     # min(D, budget) * min(K, budget) = 1600 candidates: over the fused limit
     w = WL.CONFIGS["c2"].with_(D=40, K=40, V=4096, prefix=300)
     check_step(w, rows=[(0, 0), (0, 33), (0, 64)])
 
 
-def test_step_fused_build_with_invalid_drafter_input():
+def test_step_fused_build_with_invalid_drafter_input(attn_rows):
     w = WL.CONFIGS["c2"].with_(B=3, V=4096, prefix=(70, 300))
     batch = WL.make_batch(w)
     batch.topk_logp = batch.topk_logp.copy()
@@ -121,7 +121,7 @@ def test_step_fused_build_with_invalid_drafter_input():
     assert (ref["status"][1:] & O.ST_INPUT).all() and not ref["status"][0] & O.ST_INPUT
 
 
-def test_step_fused_build_when_a_sequence_cannot_be_attended():
+def test_step_fused_build_when_a_sequence_cannot_be_attended(attn_rows):
     # sequence 1 has no room for the tree (capacity error): no cluster attends
     # it, yet its tree is still built and written
     w = WL.CONFIGS["c2"].with_(B=3, budget=8, prefix=100, V=4096, page_size=64)
@@ -132,13 +132,13 @@ def test_step_fused_build_when_a_sequence_cannot_be_attended():
     assert ref["status"][1] & O.ST_CAPACITY
 
 
-def test_step_fused_build_short_prefixes_every_tile_holds_tree_keys():
+def test_step_fused_build_short_prefixes_every_tile_holds_tree_keys(attn_rows):
     # prefixes under one key tile: every cluster waits for the tree at once
     w = WL.CONFIGS["c2"].with_(B=4, V=4096, prefix=(0, 60))
     check_step(w, rows=[(0, 0), (1, 64), (3, 17), (2, 40)])
 
 
-def test_step_fused_build_budget_zero_and_one():
+def test_step_fused_build_budget_zero_and_one(attn_rows):
     for budget in (0, 1):
         w = WL.CONFIGS["c2"].with_(B=2, V=4096, budget=budget, prefix=(64, 200))
         check_step(w)

@@ -36,7 +36,7 @@ def _inputs(w):
     ("c2", {}),                                   # the max-budget step: the key range is split
     ("c3", {"B": 6, "V": 4096, "prefix": (0, 3000)}),  # paged, variable lengths
 ])
-def test_noalloc_matches_the_workspace_entry_point_on_two_calls(cfg, mods):
+def test_noalloc_matches_the_workspace_entry_point_on_two_calls(cfg, mods, attn_rows):
     w = WL.CONFIGS[cfg].with_(**mods)
     batch, args, lay = _inputs(w)
     max_len = int(batch.prefix_len.max()) + w.Q

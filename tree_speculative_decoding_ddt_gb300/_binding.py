@@ -60,6 +60,7 @@ class StepArgs(ctypes.Structure):
 SIGNATURES = {
     "ddt_tree_build": (ctypes.c_int, [ctypes.POINTER(TreeDims)] + [_P] * 13),
     "ddt_verify_attn_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(AttnDims)]),
+    "ddt_verify_attn_rows_per_tile": (ctypes.c_int, [ctypes.POINTER(AttnDims)]),
     "ddt_verify_attn": (ctypes.c_int, [ctypes.POINTER(AttnDims)] + [_P] * 10 +
                         [ctypes.c_size_t, _P]),
     "ddt_verify_attn_noalloc": (ctypes.c_int, [ctypes.POINTER(AttnDims)] + [_P] * 10),
@@ -154,6 +155,12 @@ def attn_dims(B, Q, H, C, R, page_size, max_pages, kv_rows, dtype, scale, max_le
 
 def ddt_verify_attn_workspace_size(dims: AttnDims) -> int:
     return int(load().ddt_verify_attn_workspace_size(ctypes.byref(dims)))
+
+
+def ddt_verify_attn_rows_per_tile(dims: AttnDims) -> int:
+    """Query rows per tile (128 or 256) of the bf16 verify attention for these
+    dims on the current device; 0 for invalid or fp32 dims."""
+    return int(load().ddt_verify_attn_rows_per_tile(ctypes.byref(dims)))
 
 
 def ddt_verify_attn(q_lat, q_pe, kv_cache, block_table, prefix_len, vis_bits, scale: float,

@@ -1,6 +1,7 @@
 // Internal declarations shared by the translation units of libddt.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -80,6 +81,18 @@ cudaError_t launch_verify_attn_bf16(const ddt_attn_dims& d, const void* q_lat, c
                                     void* out, float* lse, int32_t* status, void* workspace,
                                     size_t workspace_bytes, cudaStream_t stream,
                                     const TreeFuse* fuse = nullptr);
+
+// The 256-row form of the bf16 verify attention (verify_attn_pair.cu): four-CTA
+// clusters, MMAs on paired SMs. `part_o` (bf16) / `part_lse` hold the split-KV
+// partials when n_split > 1 (merged by the caller).
+int verify_attn_pair_clusters_per_wave();
+cudaError_t launch_verify_attn_pair(const ddt_attn_dims& d, int n_split, const void* q_lat,
+                                    const void* q_pe, const void* kv, const int32_t* block_table,
+                                    const int32_t* prefix_len, const uint64_t* vis_bits, void* out,
+                                    float* lse, int32_t* status, __nv_bfloat16* part_o,
+                                    float* part_lse, cudaStream_t stream, const TreeFuse* fuse);
+// Row-tile height (128 or 256) the next bf16 launch with these dims uses.
+int verify_attn_bf16_rows_per_tile(const ddt_attn_dims& d);
 
 // Host checks of a verify-attention call (defined in ddt_api.cu).
 int check_verify_attn_args(const ddt_attn_dims* d, const void* q_lat, const void* q_pe,

@@ -42,6 +42,8 @@
 #include <math.h>
 #include <stddef.h>
 #include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include <cudaTypedefs.h>
 
@@ -920,11 +922,6 @@ __global__ void __launch_bounds__(256) k_combine(long long total_rows, int n_spl
 
 // ---------------------------------------------------------------- host side
 
-struct Plan {
-  int n_rt, n_split;
-  long long units;
-};
-
 int sm_count() {
   static int cached[64] = {};
   int dev = 0, n = 148;
@@ -934,30 +931,91 @@ int sm_count() {
   return cached[dev] ? cached[dev] : n;
 }
 
-// Split of the key range so that clusters fill whole waves: a cluster takes
-// two SMs, a wave is sm_count/2 clusters; cost ~ waves * (tiles per unit +
-// fixed overhead), plus a merge pass when the range is split.
-Plan make_plan(const ddt_attn_dims& d) {
+// One way of running a launch: the row-tile height (128: two-CTA clusters,
+// this file; 256: four-CTA clusters on paired SMs, verify_attn_pair.cu), the
+// number of key ranges each sequence is split into, and the modelled cost.
+struct Plan {
+  int rows;     // 128 or 256
+  int n_rt, n_split;
+  long long units;
+  double cost;  // in key-tile times of the 128-row kernel
+};
+
+// Cost model of a launch, in SM cycles, from cycle traces of both kernels on
+// GB300: a unit (one cluster's rows x key range) costs a fixed start (Q load,
+// instruction fetch, the first tiles through the pipeline, the epilogue) plus
+// its key tiles; units run in waves of `per_wave` clusters; a split key range
+// adds the merge pass, which streams every partial once at HBM speed.
+struct KernelCost {
+  int rows;           // query rows per tile
+  int keys_per_tile;  // keys per step of the key walk
+  double unit_start;  // cycles
+  double per_64_keys; // cycles per 64 keys of one unit
+};
+constexpr KernelCost kCost128 = {128, 64, 25000.0, 2300.0};
+constexpr KernelCost kCost256 = {256, 128, 45000.0, 2085.0};
+constexpr double kMergeBytesPerCycle = 3200.0;  // about 6.6 TB/s at 2.07 GHz
+
+Plan make_plan(const ddt_attn_dims& d, const KernelCost& k, long long per_wave) {
   Plan pl;
+  pl.rows = k.rows;
   const long long QH = (long long)d.Q * d.H;
-  pl.n_rt = (int)((QH + kBM - 1) / kBM);
+  pl.n_rt = (int)((QH + k.rows - 1) / k.rows);
   const long long base = (long long)d.B * pl.n_rt;
   const long long max_len = d.max_len > d.Q ? d.max_len : d.Q;
-  const long long n_tiles = (max_len + kBN - 1) / kBN;
-  const long long per_wave = sm_count() / 2 > 0 ? sm_count() / 2 : 1;
-  double best = 1e300;
+  const long long n_tiles = (max_len + k.keys_per_tile - 1) / k.keys_per_tile;
+  const double rows_total = (double)d.B * (double)QH;
+  if (per_wave < 1) per_wave = 1;
+  pl.cost = 1e300;
   pl.n_split = 1;
   for (long long s = 1; s <= 64 && s <= n_tiles; ++s) {
     const long long units = base * s;
     const long long waves = (units + per_wave - 1) / per_wave;
-    const double cost = (double)waves * (double)((n_tiles + s - 1) / s + 4) + (s > 1 ? 3.0 + s : 0.0);
-    if (cost < best - 1e-9) {
-      best = cost;
+    // tiles of the longest unit (the kernels give every unit but the last
+    // one tile more than an even share when the range is split)
+    const long long tpu = s > 1 ? (n_tiles + s) / s : n_tiles;
+    const double unit = k.unit_start +
+                        (double)tpu * (double)(k.keys_per_tile / 64) * k.per_64_keys;
+    const double merge =
+        s > 1 ? 3000.0 + (double)(s + 1) * rows_total * 1028.0 / kMergeBytesPerCycle : 0.0;
+    const double cost = (double)waves * unit + merge;
+    if (cost < pl.cost - 1e-9) {
+      pl.cost = cost;
       pl.n_split = (int)s;
     }
   }
   pl.units = base * pl.n_split;
   return pl;
+}
+
+Plan plan_128(const ddt_attn_dims& d) { return make_plan(d, kCost128, sm_count() / 2); }
+Plan plan_256(const ddt_attn_dims& d) {
+  int per_wave = verify_attn_pair_clusters_per_wave();
+  if (per_wave < 1) per_wave = sm_count() / 4;
+  return make_plan(d, kCost256, per_wave);
+}
+
+// The launch's plan. The 256-row kernel moves half the bytes per FLOP but
+// pads a sequence's Q*H rows to a multiple of 256: it is taken when that
+// padding is at most 1/12 of the rows (e.g. q_len 65 x 64 heads: 4160 rows
+// in 4352), else the 128-row kernel (q_len 17 x 64 heads: 1088 rows would
+// fill 1280). The environment variable DDT_VERIFY_ATTN_ROWS (128 or 256)
+// overrides the choice.
+Plan choose_plan(const ddt_attn_dims& d) {
+  const char* env = getenv("DDT_VERIFY_ATTN_ROWS");
+  if (env != nullptr && strcmp(env, "128") == 0) return plan_128(d);
+  if (env != nullptr && strcmp(env, "256") == 0) return plan_256(d);
+  const long long QH = (long long)d.Q * d.H;
+  const long long pad = ((QH + 255) / 256) * 256 - QH;
+  const bool pair_ok = verify_attn_pair_clusters_per_wave() > 0;
+  return (pair_ok && QH >= 256 && pad * 12 <= QH) ? plan_256(d) : plan_128(d);
+}
+
+size_t workspace_of(const ddt_attn_dims& d, const Plan& pl) {
+  if (pl.n_split <= 1) return 0;
+  const size_t rows = (size_t)d.B * d.Q * d.H;
+  const size_t bytes = (size_t)pl.n_split * rows * (kC * sizeof(__nv_bfloat16) + sizeof(float));
+  return (bytes + 255) & ~size_t(255);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
@@ -1011,12 +1069,11 @@ bool encode_q(CUtensorMap* ml, CUtensorMap* mp, const void* q_lat, const void* q
 
 }  // namespace
 
+// Enough for either tile height, so that the size a caller obtained stays
+// valid whichever kernel a launch picks.
 size_t verify_attn_bf16_workspace(const ddt_attn_dims& d) {
-  const Plan pl = make_plan(d);
-  if (pl.n_split <= 1) return 0;
-  const size_t rows = (size_t)d.B * d.Q * d.H;
-  const size_t bytes = (size_t)pl.n_split * rows * (kC * sizeof(__nv_bfloat16) + sizeof(float));
-  return (bytes + 255) & ~size_t(255);
+  const size_t a = workspace_of(d, plan_128(d)), b = workspace_of(d, plan_256(d));
+  return a > b ? a : b;
 }
 
 cudaError_t launch_verify_attn_bf16(const ddt_attn_dims& d, const void* q_lat, const void* q_pe,
@@ -1025,45 +1082,56 @@ cudaError_t launch_verify_attn_bf16(const ddt_attn_dims& d, const void* q_lat, c
                                     void* out, float* lse, int32_t* status, void* workspace,
                                     size_t workspace_bytes, cudaStream_t stream,
                                     const TreeFuse* fuse) {
-  const Plan pl = make_plan(d);
+  const Plan pl = choose_plan(d);
   const long long rows = (long long)d.B * d.Q * d.H;
   if (d.kv_rows < 1 || rows > 0x7fffffffLL || d.kv_rows > 0x7fffffffLL)
     return cudaErrorInvalidValue;
-  // the cache as {64 dims, rows, 9 chunks} with strides (row, 128 B)
-  CUtensorMap tm_s, tm_o, tm_ql, tm_qp;
-  if (!encode_kv_3d(&tm_s, kv, (uint64_t)d.kv_rows, kChunksPerTile) ||
-      !encode_kv_3d(&tm_o, kv, (uint64_t)d.kv_rows, 8) ||
-      !encode_q(&tm_ql, &tm_qp, q_lat, q_pe, (uint64_t)rows))
+  if (pl.n_split > 1 && (workspace == nullptr || workspace_bytes < workspace_of(d, pl)))
     return cudaErrorInvalidValue;
-
-  Params p;
-  p.B = d.B; p.Q = d.Q; p.H = d.H;
-  p.page_size = d.page_size; p.max_pages = d.max_pages; p.kv_rows = d.kv_rows;
-  p.scale_log2 = d.scale * 1.4426950408889634f;
-  p.n_rt = pl.n_rt; p.n_split = pl.n_split;
-  p.block_table = block_table; p.prefix_len = prefix_len;
-  p.vis_bits = reinterpret_cast<const unsigned long long*>(vis_bits);
-  p.q_lat = static_cast<const __nv_bfloat16*>(q_lat);
-  p.q_pe = static_cast<const __nv_bfloat16*>(q_pe);
-  p.out = static_cast<__nv_bfloat16*>(out);
-  p.lse = lse; p.status = status;
-  p.part_o = nullptr; p.part_lse = nullptr;
-  p.fuse = fuse != nullptr ? 1 : 0;
-  p.tf = fuse != nullptr ? *fuse : TreeFuse{};
+  __nv_bfloat16* part_o = nullptr;
+  float* part_lse = nullptr;
   if (pl.n_split > 1) {
-    p.part_o = static_cast<__nv_bfloat16*>(workspace);
-    p.part_lse = reinterpret_cast<float*>(p.part_o + (size_t)pl.n_split * rows * kC);
+    part_o = static_cast<__nv_bfloat16*>(workspace);
+    part_lse = reinterpret_cast<float*>(part_o + (size_t)pl.n_split * rows * kC);
   }
-  static int smem_set[64] = {};
-  cudaError_t e = ensure_smem_limit(k_verify_attn_bf16, (int)kSmemBytes, smem_set);
-  if (e != cudaSuccess) return e;
-  k_verify_attn_bf16<<<(unsigned)(pl.units * 2), kThreads, kSmemBytes, stream>>>(
-      tm_s, tm_o, tm_ql, tm_qp, p);
-  e = cudaGetLastError();
+  cudaError_t e;
+  if (pl.rows == 256) {
+    e = launch_verify_attn_pair(d, pl.n_split, q_lat, q_pe, kv, block_table, prefix_len, vis_bits,
+                                out, lse, status, part_o, part_lse, stream, fuse);
+  } else {
+    // the cache as {64 dims, rows, 9 chunks} with strides (row, 128 B)
+    CUtensorMap tm_s, tm_o, tm_ql, tm_qp;
+    if (!encode_kv_3d(&tm_s, kv, (uint64_t)d.kv_rows, kChunksPerTile) ||
+        !encode_kv_3d(&tm_o, kv, (uint64_t)d.kv_rows, 8) ||
+        !encode_q(&tm_ql, &tm_qp, q_lat, q_pe, (uint64_t)rows))
+      return cudaErrorInvalidValue;
+    Params p;
+    p.B = d.B; p.Q = d.Q; p.H = d.H;
+    p.page_size = d.page_size; p.max_pages = d.max_pages; p.kv_rows = d.kv_rows;
+    p.scale_log2 = d.scale * 1.4426950408889634f;
+    p.n_rt = pl.n_rt; p.n_split = pl.n_split;
+    p.block_table = block_table; p.prefix_len = prefix_len;
+    p.vis_bits = reinterpret_cast<const unsigned long long*>(vis_bits);
+    p.q_lat = static_cast<const __nv_bfloat16*>(q_lat);
+    p.q_pe = static_cast<const __nv_bfloat16*>(q_pe);
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.lse = lse; p.status = status;
+    p.part_o = part_o; p.part_lse = part_lse;
+    p.fuse = fuse != nullptr ? 1 : 0;
+    p.tf = fuse != nullptr ? *fuse : TreeFuse{};
+    static int smem_set[64] = {};
+    e = ensure_smem_limit(k_verify_attn_bf16, (int)kSmemBytes, smem_set);
+    if (e != cudaSuccess) return e;
+    k_verify_attn_bf16<<<(unsigned)(pl.units * 2), kThreads, kSmemBytes, stream>>>(
+        tm_s, tm_o, tm_ql, tm_qp, p);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess || pl.n_split == 1) return e;
-  k_combine<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(rows, pl.n_split, p.part_o,
-                                                            p.part_lse, p.out, lse);
+  k_combine<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(rows, pl.n_split, part_o, part_lse,
+                                                            static_cast<__nv_bfloat16*>(out), lse);
   return cudaGetLastError();
 }
+
+int verify_attn_bf16_rows_per_tile(const ddt_attn_dims& d) { return choose_plan(d).rows; }
 
 }  // namespace ddt

@@ -1,0 +1,1158 @@
+// B. Tree-verify MLA-absorb attention on paired SMs: 256-row tiles, four CTAs
+// per cluster, tcgen05 MMAs of M = 256 shared by two SMs (cta_group::2).
+//
+// "The Checkpoint: Committing a Working Native DDTree Engine", section "The
+// Message": verify attention in MLA absorb form, tree [verified_id, drafts]
+// at cache positions L + depth, mask [ones over the prefix | visibility];
+// "The Milestone Commit", section "Input Knowledge Required": the latent
+// cache of Kimi K2.6 (kv_lora_rank 512, plus a 64-wide rope part).
+//
+// Same arithmetic as the 128-row kernel (verify_attn_bf16.cu): per sequence
+// the Q*H query rows (row = query position * H + head) share one latent KV
+// head, S = [q_lat | q_pe] . [c_kv | k_pe]^T (contraction 576) and
+// O = softmax(S * scale, masked) . c_kv (output 512), online softmax, fp32
+// accumulation in TMEM. What changes is how a tile is
+// spread over the SMs. A 128 x 512 fp32 O fills the 512 TMEM columns of an
+// SM, so S and O still live on different SMs, and each side is now a pair of
+// SMs running one M = 256 MMA:
+//   * ranks 0, 1 (the S pair) hold Q rows [0,128) and [128,256) of the tile:
+//     q_lat in TMEM (256 columns), q_pe in shared memory (16 KB). S is taken
+//     over 128-key tiles: each S-CTA loads one 64-key half of the tile (64
+//     keys x 576 dims, 72 KB) and the pair MMA (issued by rank 0; N = 128, so
+//     36 MMA instructions per 128 keys) writes S for its 128 rows x all 128
+//     keys into each CTA's TMEM (two 128-column buffers). Eight softmax warps
+//     per CTA take two threads per row, one per 64-key half; each half ships
+//     its P block (bf16, 16 KB) plus per-row rescale factors to the O-CTA of
+//     the same rows;
+//   * ranks 2, 3 (the O pair) hold O rows [0,128) and [128,256) in TMEM and
+//     consume the P blocks in key order, 64 keys at a time: each loads HALF of
+//     the value dims of the block (64 keys x 256 dims, 32 KB: rank 2 dims
+//     [0,128) and [256,384), rank 3 the other two) and the pair MMA (issued
+//     by rank 2) accumulates O += P V.
+// Against one 128-row tile per SM pair this halves the bytes every CTA stages
+// per FLOP and the L2 traffic of the key walk. A single thread issues a
+// tcgen05.mma with A in TMEM only about every 70 cycles whatever N is, so the
+// S tile is as wide as TMEM allows (N = 128) to keep the MMA count per key low.
+//
+// Warp roles (352 threads). S-CTAs: warp 0 TMA (its Q rows, then its key
+// halves), warp 1 TMEM allocation and (rank 0) the first MMA issuer, warps
+// 2-9 softmax (warp w: lane quadrant w % 4, key half (w - 2) / 4), warp 10
+// (rank 0) the second MMA issuer (the two take alternate key tiles, which
+// keeps the tensor pipe busy while one of them is issuing). O-CTAs: warp 0
+// TMA, warp 1 TMEM allocation and (rank 2) the PV issuer, warps 2-5 row warps
+// (rescales, output), warp 6 of rank 2 the fused tree build.
+#include <cuda_bf16.h>
+#include <math.h>
+#include <stddef.h>
+#include <stdio.h>
+
+#include <cudaTypedefs.h>
+
+#include "ddt_internal.cuh"
+#include "sm100_ptx.cuh"
+#include "tree_build_warp.cuh"
+
+namespace ddt {
+namespace {
+
+using namespace sm100;
+
+constexpr int kTM = 256;  // query rows per tile
+constexpr int kHM = 128;  // query rows per CTA
+constexpr int kBK = 64;   // keys per block (one P message, one value stage)
+constexpr int kBS = 128;  // keys per S tile (two blocks; one per S-CTA)
+constexpr int kC = 512;
+constexpr int kR = 64;
+constexpr int kThreads = 352;
+constexpr int kStagesK = 2;   // S-CTA key stages (one 64-key half of an S tile each)
+constexpr int kStagesV = 4;   // O-CTA value stages (one 64-key block each)
+constexpr int kStageSlots = 3;  // S-CTA: outgoing P blocks (free once copied)
+constexpr int kMsgSlots = 4;    // O-CTA: incoming P blocks (free once PV has read them)
+
+constexpr int kChunks = (kC + kR) / 64;                   // 9 chunks of 64 dims
+constexpr uint32_t kKChunk = kBK * 128;                   // 64 keys x 128 B
+constexpr uint32_t kTileK = kChunks * kKChunk;            // an S-CTA's key half: 72 KB
+constexpr uint32_t kVChunk = kBK * 128;                   // 64 keys x 128 B
+constexpr uint32_t kTileV = 4 * kVChunk;                  // an O-CTA's value half: 32 KB
+constexpr uint32_t kPBytes = kHM * 128;                   // P: 128 rows x 64 keys bf16
+constexpr uint32_t kMsgBytes = kPBytes + kHM * 4 + 16;    // P | per-row factor | 4 warp flags
+constexpr uint32_t kMsgStride = 17408;
+constexpr uint32_t kFinBytes = kHM * 4;
+constexpr uint32_t kQlBytes = kHM * kC * 2;               // q_lat rows: 128 KB
+constexpr uint32_t kQpBytes = kHM * kR * 2;               // q_pe rows: 16 KB
+constexpr uint32_t kOutStride = 1040;
+
+// S-CTA shared memory
+constexpr uint32_t S_RING = 0;
+constexpr uint32_t S_QPE = S_RING + kStagesK * kTileK;   // q_pe (SW128, K-major)
+constexpr uint32_t S_STAGE = S_QPE + kQpBytes;            // outgoing messages
+constexpr uint32_t S_FIN = S_STAGE + kStageSlots * kMsgStride;
+constexpr uint32_t S_XCH = S_FIN + 1024;   // running max handoff [128], final (m, l) [2][128][2]
+constexpr uint32_t S_VIS = S_XCH + 2048 + 512;   // ancestor words of the fused build [kMaxQ][kMaxW]
+constexpr uint32_t S_END = S_VIS + kMaxQ * kMaxW * 8;
+// O-CTA shared memory
+constexpr uint32_t O_RING = 0;
+constexpr uint32_t O_MSG = O_RING + kStagesV * kTileV;
+constexpr uint32_t O_FIN = O_MSG + kMsgSlots * kMsgStride;
+constexpr uint32_t O_GO = O_FIN + 512;  // message index of the current GO call (-1: the end)
+constexpr uint32_t O_BUILD = O_FIN + 1024;
+constexpr uint32_t kBuildBytes = (uint32_t)tb::smem_bytes(kFuseMaxCand, 1);
+constexpr uint32_t O_END = O_BUILD + ((kBuildBytes + 1023) & ~1023u);
+
+constexpr int kBtMax = 1024;
+constexpr uint32_t OFF_BT = (S_END > O_END ? S_END : O_END);
+constexpr uint32_t OFF_BAR = OFF_BT + kBtMax * 4;
+constexpr uint32_t kSmemBytes = OFF_BAR + 1024 + 1024;
+static_assert(kQlBytes <= kStagesK * kTileK, "q_lat is staged in the S-CTA ring");
+static_assert(S_STAGE % 1024 == 0 && O_MSG % 1024 == 0 && kMsgStride % 1024 == 0, "alignment");
+static_assert(kMsgBytes <= kMsgStride && kMsgBytes % 16 == 0, "message size");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+static_assert(kHM * kOutStride <= O_FIN, "the output is staged in the O-CTA ring and messages");
+static_assert(S_QPE % 1024 == 0, "q_pe is an MMA operand");
+static_assert(offsetof(tb::Smem, anc) % 16 == 0, "ancestor words are bulk-copied");
+
+enum Bar {
+  // S-CTAs
+  B_RING_FULL = 0,                        // +stage; this CTA's key half landed
+  B_RING_PEER = B_RING_FULL + kStagesK,   // +stage; rank 0: rank 1's key half landed (relay)
+  B_RING_EMPTY = B_RING_PEER + kStagesK,  // +stage; both (pair MMA commit)
+  B_S_FULL = B_RING_EMPTY + kStagesK,     // +buffer; both (pair MMA commit)
+  B_S_EMPTY = B_S_FULL + 2,               // +buffer; rank 0: the 8 warps of one group
+  B_Q_FULL = B_S_EMPTY + 2,               // this CTA's Q rows landed
+  B_Q_TMEM = B_Q_FULL + 1,                // rank 0: 16 warps, rank 1: 8
+  B_P_FREE = B_Q_TMEM + 1,                // +O-CTA slot; both (PV commit from rank 2)
+  B_STAGE_FREE = B_P_FREE + kMsgSlots,    // +staging slot; the O-CTA saw the copy land
+  B_TREE = B_STAGE_FREE + kStageSlots,    // ancestor words of the fused build
+  // O-CTAs
+  B_HALF_FULL = B_TREE + 1,               // +stage; this CTA's value half landed
+  B_HALF_PEER = B_HALF_FULL + kStagesV,   // +stage; rank 2: rank 3's value half landed (relay)
+  B_HALF_EMPTY = B_HALF_PEER + kStagesV,  // +stage; both (PV commit)
+  B_P_FULL = B_HALF_EMPTY + kStagesV,     // +slot; completed by the S-CTA's copy
+  B_P_PEER = B_P_FULL + kMsgSlots,        // +slot; rank 2: rank 3's message landed (relay)
+  B_PV_DONE = B_P_PEER + kMsgSlots,       // +slot; both (PV commit)
+  B_GO = B_PV_DONE + kMsgSlots,           // both: the PV issuer calls the row warps (a rescale, or the end)
+  B_O_READY = B_GO + 1,                   // rank 2: +0 its row warps, +1 rank 3's, rescale done
+  B_FIN_FULL = B_O_READY + 2,
+  B_TAIL_OK = B_FIN_FULL + 1,             // rank 2: both halves of the last block zeroed
+  // both sides
+  B_MMA_DONE = B_TAIL_OK + 1,
+  N_BARS = B_MMA_DONE + 1
+};
+static_assert(N_BARS * 8 + 16 <= 1024, "barrier area");
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemQ = 0;    // S-CTA: q_lat [0,256)
+constexpr uint32_t kTmemS = 256;  // S-CTA: S buffers [256,384), [384,512)
+
+constexpr uint32_t kIdescS = idesc_bf16_f32(kTM, kBS, false);
+constexpr uint32_t kIdescPV = idesc_bf16_f32(kTM, 256, true);
+constexpr uint16_t kMaskS = 0x3;  // ranks 0, 1
+constexpr uint16_t kMaskO = 0xC;  // ranks 2, 3
+
+struct Params {
+  int B, Q, H;
+  int page_size, max_pages;
+  long long kv_rows;
+  float scale_log2;
+  int n_rt, n_split;
+  const int32_t* block_table;
+  const int32_t* prefix_len;
+  const unsigned long long* vis_bits;
+  __nv_bfloat16* out;
+  float* lse;
+  int32_t* status;
+  __nv_bfloat16* part_o;
+  float* part_lse;
+  int fuse;
+  TreeFuse tf;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src_cta,
+                                                  uint32_t bytes, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst_cluster),
+      "r"(src_cta), "r"(bytes), "r"(bar_cluster)
+      : "memory");
+}
+// named barrier 1 over `n` threads, returning the AND of `ok` over them
+__device__ __forceinline__ bool bar1_and(bool ok, uint32_t n) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.and.pred po, 1, %2, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)ok), "r"(n)
+      : "memory");
+  return r != 0;
+}
+// named barrier `id` over `n` threads, returning the AND of `ok` over them
+__device__ __forceinline__ bool bar1_and_id(bool ok, uint32_t id, uint32_t n) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.and.pred po, %2, %3, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)ok), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+// Rows of this CTA written as empty (capacity / range errors, empty splits):
+// the O-CTAs write zero output, the S-CTAs write lse = -inf.
+__device__ void write_empty(const Params& p, int b, int rt, int sp, uint32_t rank) {
+  const int QH = p.Q * p.H;
+  const long long total = (long long)p.B * QH;
+  const int half = (int)(rank & 1u);
+  for (int e = threadIdx.x; e < kHM * 64; e += kThreads) {
+    const int r = e >> 6, c = e & 63;
+    const int lr = rt * kTM + half * kHM + r;
+    if (lr >= QH) continue;
+    const long long grow = (long long)b * QH + lr;
+    if (rank >= 2) {
+      __nv_bfloat16* dst = p.n_split == 1 ? p.out + grow * kC
+                                          : p.part_o + ((long long)sp * total + grow) * kC;
+      reinterpret_cast<uint4*>(dst)[c] = make_uint4(0, 0, 0, 0);
+    } else if (c == 0) {
+      if (p.n_split == 1) {
+        if (p.lse) p.lse[grow] = -INFINITY;
+      } else {
+        p.part_lse[(long long)sp * total + grow] = -INFINITY;
+      }
+    }
+  }
+}
+
+__device__ int fused_build(const TreeFuse& f, int b, unsigned char* bsm, bool* bad) {
+  const int De = min(f.D, f.budget), Ke = min(f.K, f.budget);
+  tb::Smem& S = *reinterpret_cast<tb::Smem*>(bsm);
+  double* s_logp = reinterpret_cast<double*>(bsm + sizeof(tb::Smem));
+  int32_t* s_ids = reinterpret_cast<int32_t*>(s_logp + De * Ke);
+  const float* lp = f.topk_logp + (size_t)b * f.D * f.K;
+  const int32_t* ip = f.topk_ids + (size_t)b * f.D * f.K;
+  const int32_t root = f.root_tok[b];
+  switch (tb::slots_for(f.budget + 1)) {
+    case 1: return tb::build_warp<1>(lp, ip, root, f.D, f.K, f.budget, f.V, De, Ke, S, s_logp, s_ids, bad);
+    case 2: return tb::build_warp<2>(lp, ip, root, f.D, f.K, f.budget, f.V, De, Ke, S, s_logp, s_ids, bad);
+    case 3: return tb::build_warp<3>(lp, ip, root, f.D, f.K, f.budget, f.V, De, Ke, S, s_logp, s_ids, bad);
+    default: return tb::build_warp<4>(lp, ip, root, f.D, f.K, f.budget, f.V, De, Ke, S, s_logp, s_ids, bad);
+  }
+}
+__device__ void fused_write(const Params& p, int b, const unsigned char* bsm, int n, bool bad) {
+  const TreeFuse& f = p.tf;
+  const int32_t st = tb::write_warp(*reinterpret_cast<const tb::Smem*>(bsm), b, f.budget + 1, n,
+                                    bad, f.tokens, f.parents, f.depths,
+                                    reinterpret_cast<unsigned long long*>(f.vis_bits), f.vis,
+                                    f.first_child, f.next_sibling, f.n_nodes);
+  if ((threadIdx.x & 31) == 0 && st != 0) atomicOr(p.status + b, st);
+}
+
+__global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
+    k_verify_attn_pair(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_ql,
+                       const __grid_constant__ CUtensorMap tm_qp, const Params p) {
+  extern __shared__ __align__(1024) unsigned char smem_dyn[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + N_BARS * 8);
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+
+  const uint32_t rank = cluster_rank();
+  const bool s_side = rank < 2;
+  const int half = (int)(rank & 1u);  // which 128 rows of the tile this CTA holds
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  const long long unit = blockIdx.x >> 2;
+  const int sp = (int)(unit % p.n_split);
+  const int rt = (int)((unit / p.n_split) % p.n_rt);
+  const int b = (int)(unit / ((long long)p.n_split * p.n_rt));
+  const int QH = p.Q * p.H;
+  const long long total_rows = (long long)p.B * QH;
+  const int32_t* bt = p.block_table + (size_t)b * p.max_pages;
+  const long long row0 = (long long)b * QH + (long long)rt * kTM + half * kHM;  // this CTA's rows
+
+  // Q depends on no check: each S-CTA starts the load of its 128 rows first
+  // (q_lat into the key ring, which the keys take over once it is in TMEM;
+  // q_pe into its own area, where it stays as an MMA operand)
+  if (s_side && tid == 0) {
+    mbar_init(bar(B_Q_FULL), 1);
+    fence_mbar_init();
+    mbar_expect_tx(bar(B_Q_FULL), kQlBytes + kQpBytes);
+    tma_load_3d(sbase + S_RING, &tm_ql, 0, (int)row0, 0, bar(B_Q_FULL));
+    tma_load_2d(sbase + S_QPE, &tm_qp, 0, (int)row0, bar(B_Q_FULL));
+  }
+
+  // ---- capacity and page checks: identical decision in all four CTAs ------
+  const long long L = p.prefix_len[b];
+  const long long n_keys = L + p.Q;
+  int32_t* s_bt = reinterpret_cast<int32_t*>(smem + OFF_BT);
+  int code = 0;
+  if (L < 0 || n_keys > (long long)p.max_pages * p.page_size) code = DDT_ST_CAPACITY;
+  if (code == 0) {
+    const long long n_pages = (n_keys + p.page_size - 1) / p.page_size;
+    const long long kv_pages = p.kv_rows / p.page_size;
+    bool badp = false;
+    for (long long q = tid; q < n_pages; q += kThreads) {
+      const int32_t pg = bt[q];
+      if (q < kBtMax) s_bt[q] = pg;
+      if (pg < 0 || pg >= kv_pages) badp = true;
+    }
+    if (__syncthreads_or(badp)) code = DDT_ST_RANGE;
+  }
+  const int n_tiles = (int)((n_keys + kBS - 1) / kBS);   // 128-key S tiles
+  const int n_blocks = (int)((n_keys + kBK - 1) / kBK);  // 64-key blocks
+  // the last unit of a split sequence also walks the tree tiles (and builds
+  // the tree): the earlier units take the extra tile when the range divides
+  const int tps = p.n_split > 1 ? (n_tiles + p.n_split) / p.n_split : n_tiles;
+  const int j_begin = sp * tps;
+  const int nt = code ? 0 : max(0, min(n_tiles, j_begin + tps) - j_begin);
+  const int sp_last = code ? 0 : (n_tiles - 1) / tps;
+  const bool designated = p.fuse && rt == 0 && sp == sp_last;
+  // The sequence's last S tile may hold one 64-key block only; its second
+  // half is then a phantom: loaded from the first half's rows, fully masked,
+  // never sent. Message m of the unit is block 2 * tile_of(m / 2) + m % 2.
+  const bool phantom = nt > 0 && j_begin + nt == n_tiles && 2 * n_tiles > n_blocks;
+  const int n_msgs = 2 * nt - (phantom ? 1 : 0);
+  if (nt == 0) {
+    if (s_side && tid == 0) mbar_wait(bar(B_Q_FULL), 0);  // nothing lands after exit
+    write_empty(p, b, rt, sp, rank);
+    if (code && rt == 0 && sp == 0 && rank == 0 && tid == 0) atomicOr(p.status + b, code);
+    if (designated && rank == 2 && warp == 6) {
+      bool bad = false;
+      const int n = fused_build(p.tf, b, smem + O_BUILD, &bad);
+      fused_write(p, b, smem + O_BUILD, n, bad);
+    }
+    return;  // all four CTAs of the cluster take this branch together
+  }
+  // Key walk (as in the 128-row kernel): tiles wholly inside the prefix from a
+  // staggered starting point, the tiles holding tree keys last, in order.
+  const int n_pure = (int)(L / kBS);
+  const int nrot = max(0, min(j_begin + nt, n_pure) - j_begin);
+  const bool builds = p.fuse && nt > nrot;
+  const uint32_t vis_bytes = (uint32_t)(p.Q * kMaxW * 8);
+
+  // ---- setup ---------------------------------------------------------------
+  if (tid == 0) {
+    if (s_side) {
+      for (int s = 0; s < kStagesK; ++s) {
+        mbar_init(bar(B_RING_FULL + s), 1);
+        mbar_init(bar(B_RING_PEER + s), 1);
+        mbar_init(bar(B_RING_EMPTY + s), 1);
+      }
+      for (int s = 0; s < 2; ++s) {
+        mbar_init(bar(B_S_FULL + s), 1);
+        mbar_init(bar(B_S_EMPTY + s), 8);
+      }
+      for (int s = 0; s < kMsgSlots; ++s) mbar_init(bar(B_P_FREE + s), 1);
+      for (int s = 0; s < kStageSlots; ++s) mbar_init(bar(B_STAGE_FREE + s), 1);
+      mbar_init(bar(B_Q_TMEM), rank == 0 ? 16 : 8);
+      mbar_init(bar(B_MMA_DONE), 2);
+      if (builds) {
+        mbar_init(bar(B_TREE), 1);
+        mbar_expect_tx(bar(B_TREE), vis_bytes);
+      }
+    } else {
+      for (int s = 0; s < kStagesV; ++s) {
+        mbar_init(bar(B_HALF_FULL + s), 1);
+        mbar_init(bar(B_HALF_PEER + s), 1);
+        mbar_init(bar(B_HALF_EMPTY + s), 1);
+      }
+      for (int s = 0; s < kMsgSlots; ++s) {
+        mbar_init(bar(B_P_FULL + s), 1);
+        mbar_init(bar(B_P_PEER + s), 1);
+        mbar_init(bar(B_PV_DONE + s), 1);
+      }
+      mbar_init(bar(B_GO), 1);
+      mbar_init(bar(B_O_READY + 0), 4);
+      mbar_init(bar(B_O_READY + 1), 4);
+      mbar_init(bar(B_FIN_FULL), 1);
+      mbar_init(bar(B_TAIL_OK), 2);
+      mbar_init(bar(B_MMA_DONE), 1);
+      for (int s = 0; s < kMsgSlots && s < n_msgs; ++s)
+        mbar_expect_tx(bar(B_P_FULL + s), kMsgBytes);
+      mbar_expect_tx(bar(B_FIN_FULL), kFinBytes);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish_pair();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  cluster_sync();  // every barrier and TMEM allocation of the cluster exists before any remote use
+
+  bool failed = false;
+  const int rot = nrot > 0 ? (int)(((long long)rt * nrot) / p.n_rt) : 0;
+  auto tile_of = [&](int jj) -> int {
+    return (jj < nrot) ? j_begin + (jj + rot) % nrot : j_begin + jj;
+  };
+  // cache row of the first key of 64-key block `blk` of the sequence
+  auto block_row = [&](int blk) -> long long {
+    const long long t0 = (long long)blk * kBK;
+    const long long pi = t0 / p.page_size;
+    const int32_t pg = pi < kBtMax ? s_bt[pi] : bt[pi];
+    return (long long)pg * p.page_size + t0 % p.page_size;
+  };
+  auto msg_block = [&](int m) -> int { return 2 * tile_of(m >> 1) + (m & 1); };
+
+  if (s_side) {
+    // ========================= S-CTAs =========================
+    if (warp == 0) {
+      if (lane == 0) {
+        prefetch_tmap(&tm_k);
+        int u = 0;
+        if (!mbar_wait_cluster(bar(B_Q_TMEM), 0)) failed = true;  // q_lat has left the ring
+        if (!mbar_wait(bar(B_Q_FULL), 0)) failed = true;
+        for (; u < nt && !failed; ++u) {  // this CTA's 64-key half of tile u, one request
+          const int slot = u % kStagesK;
+          if (u >= kStagesK &&
+              !mbar_wait_cluster(bar(B_RING_EMPTY + slot), ((u / kStagesK) - 1) & 1)) {
+            failed = true;
+            break;
+          }
+          mbar_expect_tx(bar(B_RING_FULL + slot), kTileK);
+          int blk = 2 * tile_of(u) + half;
+          if (blk >= n_blocks) blk -= 1;  // the phantom half: the other half's rows
+          tma_load_3d(sbase + S_RING + slot * kTileK, &tm_k, 0, (int)block_row(blk), 0,
+                      bar(B_RING_FULL + slot));
+        }
+        // nothing may land after the CTAs leave
+        for (int v = max(0, u - kStagesK); v < u; ++v)
+          if (!mbar_wait(bar(B_RING_FULL + v % kStagesK), (v / kStagesK) & 1)) failed = true;
+      }
+    } else if (rank == 0 && (warp == 1 || warp == 10)) {
+      // QK^T for both S-CTAs over 128 keys: q_lat from TMEM (TS), q_pe from
+      // shared memory (SS), B = the two 64-key halves, D = S (128 x 128 in
+      // each CTA). Tile jj uses S buffer and key stage jj & 1.
+      if (lane == 0) {
+        const int first = warp == 1 ? 0 : 1;
+        if (!mbar_wait_cluster(bar(B_Q_TMEM), 0)) failed = true;
+        tc_fence_after();
+        for (int jj = first; jj < nt && !failed; jj += 2) {
+          const int sb = jj & 1;
+          if (jj >= 2 && !mbar_wait_cluster(bar(B_S_EMPTY + sb), ((jj >> 1) - 1) & 1)) {
+            failed = true;
+            break;
+          }
+          const int slot = jj % kStagesK;
+          if (!mbar_wait(bar(B_RING_FULL + slot), (jj / kStagesK) & 1) ||
+              !mbar_wait_cluster(bar(B_RING_PEER + slot), (jj / kStagesK) & 1)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem + kTmemS + sb * kBS;
+          const uint32_t st = sbase + S_RING + slot * kTileK;
+#pragma unroll
+          for (int c = 0; c < kC / 64; ++c) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t bd = smem_desc(st + c * kKChunk + kk * 32, 16, 1024, kSwizzle128B);
+              umma_pair_bf16_ts(d, tmem + kTmemQ + 32 * c + 8 * kk, bd, kIdescS,
+                                (c | kk) ? 1u : 0u);
+            }
+          }
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = smem_desc(sbase + S_QPE + kk * 32, 16, 1024, kSwizzle128B);
+            const uint64_t bd =
+                smem_desc(st + (kC / 64) * kKChunk + kk * 32, 16, 1024, kSwizzle128B);
+            umma_pair_bf16(d, ad, bd, kIdescS, 1u);
+          }
+          umma_pair_commit(bar(B_RING_EMPTY + slot), kMaskS);
+          umma_pair_commit(bar(B_S_FULL + sb), kMaskS);
+        }
+        umma_pair_commit(bar(B_MMA_DONE), 0x1);
+        if (!mbar_wait(bar(B_MMA_DONE), 0)) failed = true;
+      }
+    } else if (rank == 1 && warp == 10) {
+      // relay: this CTA's key half of tile u has landed -> rank 0's MMA issuers
+      // (each CTA's tile loads complete on its own barrier; a load that signals
+      // the peer's barrier directly slows this CTA's outgoing P copies)
+      if (lane == 0) {
+        const uint32_t peer0 = map_peer(bar(B_RING_PEER), 0);
+        for (int u = 0; u < nt; ++u) {
+          if (!mbar_wait(bar(B_RING_FULL + u % kStagesK), (u / kStagesK) & 1)) {
+            failed = true;
+            break;
+          }
+          mbar_arrive_cluster(peer0 + 8 * (u % kStagesK));
+        }
+      }
+    } else if (warp >= 2 && warp <= 9) {
+      // ---------------- softmax: two groups of four warps, alternate tiles ----
+      // Group g (warps 2-5: g = 0, warps 6-9: g = 1) takes the tiles jj with
+      // jj % 2 == g (so also S buffer g), one thread per row over all 128
+      // keys. The only thing that passes from tile to tile is each row's
+      // running max, handed from one group to the other through shared
+      // memory and a named barrier per (lane quadrant, direction); the
+      // exponentials of consecutive tiles run in the two groups at once.
+      // Every handoff is made whatever happens (a group that gave up on a
+      // wait skips its work, not its barriers), so neither group can be left
+      // waiting for the other.
+      const int qd = warp & 3;
+      const int g = (warp - 2) >> 2;
+      const int r = qd * 32 + lane;
+      const uint32_t t_lane = tmem + ((uint32_t)(qd * 32) << 16);
+      const int lr = rt * kTM + half * kHM + r;
+      const bool row_ok = lr < QH;
+      const int qi = row_ok ? lr / p.H : 0;
+      const int W = (p.Q + 63) >> 6;
+      float* hand = reinterpret_cast<float*>(smem + S_XCH);  // [row]: running max handoff
+      float* fin = hand + kHM;                               // [group][row][2]: (m, l) at the end
+      unsigned long long vis0 = 0ull, vis1 = 0ull;
+      bool vis_ready = !p.fuse;
+      if (!p.fuse && row_ok) {
+        const unsigned long long* vb = p.vis_bits + ((size_t)b * p.Q + qi) * W;
+        vis0 = vb[0];
+        if (W > 1) vis1 = vb[1];
+      }
+      // q_lat row r -> TMEM columns [0,256) (bf16 pairs); group 0 moves
+      // chunks 0-3, group 1 chunks 4-7
+      const bool q_ok = __all_sync(0xffffffffu, mbar_wait(bar(B_Q_FULL), 0));
+      if (q_ok) {
+        const unsigned char* qrow = smem + S_RING + r * 128;
+#pragma unroll 1
+        for (int c = 4 * g; c < 4 * g + 4; ++c) {
+          uint32_t v[32];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint4 x = *reinterpret_cast<const uint4*>(qrow + c * (kHM * 128) +
+                                                             ((q ^ (r & 7)) << 4));
+            v[4 * q + 0] = x.x;
+            v[4 * q + 1] = x.y;
+            v[4 * q + 2] = x.z;
+            v[4 * q + 3] = x.w;
+          }
+          tmem_st32(t_lane + kTmemQ + 32 * c, v);
+        }
+        tmem_st_wait();
+      }
+      fence_proxy_async_smem();  // the ring is refilled by TMA after this
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(B_Q_TMEM));
+        if (rank == 1) mbar_arrive_cluster(map_peer(bar(B_Q_TMEM), 0));
+      }
+      if (!bar1_and(q_ok, 256)) failed = true;
+      const uint32_t msg_peer0 = map_peer(sbase + O_MSG, rank + 2);
+      const uint32_t pfull_peer0 = map_peer(bar(B_P_FULL), rank + 2);
+      const uint32_t s_empty0 = map_peer(bar(B_S_EMPTY), 0);
+      const uint32_t bar_in = 2 + 2 * qd + g;         // handoff to this group
+      const uint32_t bar_out = 2 + 2 * qd + (g ^ 1);  // handoff to the other group
+      const uint32_t bar_grp = 10 + g;                // the group's four warps
+
+      const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+      float m_run = -INFINITY;  // the row's running max (scaled, log2 units)
+      float m_l = -INFINITY;    // reference max of this group's partial sum
+      float l_run = 0.f;        // this group's share of the row sum, relative to m_l
+      int rj = rot;
+      for (int jj = 0; jj < nt; ++jj) {
+        const int tile = jj < nrot ? j_begin + rj : j_begin + jj;
+        if (jj < nrot && ++rj == nrot) rj = 0;
+        if ((jj & 1) != g) continue;
+        bool ok = !failed;
+        float x[128];  // raw scores q.k of the tile's 128 keys
+        if (ok) {
+          ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar(B_S_FULL + g), (jj >> 1) & 1));
+          tc_fence_after();
+          uint32_t sa[32];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            tmem_ld32(t_lane + kTmemS + g * kBS + 32 * q, sa);
+            tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) x[32 * q + k] = __uint_as_float(sa[k]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (rank == 0) mbar_arrive(bar(B_S_EMPTY + g));
+            else mbar_arrive_cluster(s_empty0 + 8 * g);
+          }
+#pragma unroll
+          for (int kb = 0; kb < 2; ++kb) {
+            const int blk = 2 * tile + kb;
+            const long long t0 = (long long)blk * kBK;
+            unsigned long long m = ~0ull;  // visible keys of the block
+            if (blk >= n_blocks) {
+              m = 0ull;  // the phantom block
+            } else if (t0 + kBK > L) {
+              if (!vis_ready) {
+                ok = ok && __all_sync(0xffffffffu, mbar_wait_cluster(bar(B_TREE), 0));
+                if (row_ok) {
+                  const unsigned long long* vw =
+                      reinterpret_cast<const unsigned long long*>(smem + S_VIS) + qi * kMaxW;
+                  vis0 = vw[0];
+                  vis1 = vw[1];
+                }
+                vis_ready = true;
+              }
+              // key k is slot t0 + k; slots below L are prefix, slot L + t is
+              // tree slot t (bit t of vis1:vis0), slots from n_keys on do not exist
+              const int np = (int)max(0ll, L - t0);
+              const int off = (int)(t0 - L);
+              const int nk = (int)min(64ll, n_keys - t0);
+              unsigned long long tm;
+              if (off < 0) tm = vis0 << (-off);
+              else if (off == 0) tm = vis0;
+              else if (off < 64) tm = (vis0 >> off) | (vis1 << (64 - off));
+              else tm = vis1 >> (off - 64);
+              const unsigned long long pm = (1ull << np) - 1ull;
+              const unsigned long long km = nk >= 64 ? ~0ull : (1ull << nk) - 1ull;
+              m = (pm | tm) & km;
+            }
+            if (m != ~0ull) {
+#pragma unroll
+              for (int k = 0; k < 64; ++k)
+                if (!((m >> k) & 1ull)) x[64 * kb + k] = -INFINITY;
+            }
+          }
+        }
+        float mt = -INFINITY;
+        if (ok) {
+          float mx8[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) mx8[q] = x[q];
+#pragma unroll
+          for (int k = 8; k < 128; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], x[k]);
+          // the scale is positive, so it commutes with the max
+          mt = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                     fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
+               p.scale_log2;
+        }
+        // running max after the previous tile, from the other group
+        if (jj > 0) {
+          asm volatile("bar.sync %0, 64;" ::"r"(bar_in) : "memory");
+          m_run = hand[r];
+        }
+        // lazy rescale: the reference max moves only when the row max passes it
+        // by 8 (a factor 2^8); O on the peer is then multiplied by `factor`
+        // before the tile's first block is added
+        float factor = 1.f;
+        bool rescale = false;
+        if (mt > m_run + 8.f) {
+          factor = ex2(m_run - mt);  // 0 when m_run is -inf
+          rescale = jj > 0;
+          m_run = mt;
+        }
+        if (jj + 1 < nt) {
+          hand[r] = m_run;
+          asm volatile("bar.arrive %0, 64;" ::"r"(bar_out) : "memory");
+        }
+        // Exponentials, P blocks and their copies. The group barriers run
+        // whatever `ok` is (a warp that gave up skips the work, not the
+        // barriers); the phantom block is skipped by the whole group.
+        if (ok && m_run != m_l) {
+          if (l_run != 0.f) l_run *= ex2(m_l - m_run);
+          m_l = m_run;
+        }
+        // p = 2^(x * scale*log2(e) - m); every x is -inf while m is -inf: p = 0
+        const float nm = m_run == -INFINITY ? 0.f : -m_run;
+        const float2 neg_m = make_float2(nm, nm);
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+          if (2 * tile + kb >= n_blocks) continue;
+          const int msg_i = 2 * jj + kb;
+          const int ss = msg_i % kStageSlots;
+          if (ok && msg_i >= kStageSlots)
+            ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar(B_STAGE_FREE + ss),
+                                                           ((msg_i / kStageSlots) - 1) & 1));
+          if (ok) {
+            unsigned char* msg = smem + S_STAGE + ss * kMsgStride;
+            const uint32_t p_row =
+                sbase + S_STAGE + ss * kMsgStride + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {  // 8 keys -> one 16-byte unit of the row
+              uint32_t pk[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int k = 64 * kb + 8 * c + 2 * e;
+                const float2 ex = ffma2(make_float2(x[k], x[k + 1]), sl2, neg_m);
+                const float2 pp = make_float2(ex2(ex.x), ex2(ex.y));
+                pk[e] = pack_bf16(pp.x, pp.y);
+                acc[e] = fadd2(acc[e], pp);
+              }
+              const uint32_t addr = p_row + ((uint32_t)(c ^ (r & 7)) << 4);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[0]),
+                           "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
+                           : "memory");
+            }
+            // the rescale travels with the tile's first block only
+            if (kb == 0) reinterpret_cast<float*>(msg + kPBytes)[r] = rescale ? factor : 1.f;
+            const bool any_rescale = kb == 0 && __any_sync(0xffffffffu, rescale);
+            if (lane == 0) reinterpret_cast<uint32_t*>(msg + kPBytes + kHM * 4)[qd] = any_rescale;
+            fence_proxy_async_smem();
+          }
+          // the group's four warps have written the block: one thread sends it,
+          // once PV has released the O-CTA slot it goes to
+          const bool all_ok = bar1_and_id(ok, bar_grp, 128);
+          if (!all_ok) ok = false;
+          if (all_ok && lane == 0 && warp == 2 + 4 * g) {
+            const int mb = msg_i % kMsgSlots;
+            if (msg_i < kMsgSlots ||
+                mbar_wait_cluster(bar(B_P_FREE + mb), ((msg_i / kMsgSlots) - 1) & 1))
+              bulk_copy_to_peer(msg_peer0 + mb * kMsgStride, sbase + S_STAGE + ss * kMsgStride,
+                                kMsgBytes, pfull_peer0 + 8 * mb);
+            else
+              ok = false;
+          }
+        }
+        if (ok) {
+          const float2 a = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+          l_run += a.x + a.y;
+        }
+        // a wait that gave up in any warp of the group stops the whole group
+        if (!bar1_and_id(ok, bar_grp, 128)) failed = true;
+      }
+
+      // ---- finish: the row sum over both groups, lse here, 1/l to the O-CTA --
+      fin[(g * kHM + r) * 2 + 0] = m_l;
+      fin[(g * kHM + r) * 2 + 1] = l_run;
+      asm volatile("bar.sync %0, 64;" ::"r"(12 + qd) : "memory");
+      const bool all_ok = bar1_and(!failed, 256);
+      if (all_ok && g == 0) {
+        const float ma = fin[r * 2 + 0], la = fin[r * 2 + 1];
+        const float mb2 = fin[(kHM + r) * 2 + 0], lb = fin[(kHM + r) * 2 + 1];
+        const float mf = fmaxf(ma, mb2);
+        float l_tot = 0.f;
+        if (la != 0.f) l_tot += la * ex2(ma - mf);
+        if (lb != 0.f) l_tot += lb * ex2(mb2 - mf);
+        const bool live = l_tot > 0.f;
+        const long long grow = row0 + r;
+        if (row_ok) {
+          const float lse_v = live ? (mf + __log2f(l_tot)) * 0.69314718055994530942f : -INFINITY;
+          if (p.n_split == 1) {
+            if (p.lse) p.lse[grow] = lse_v;
+          } else {
+            p.part_lse[(long long)sp * total_rows + grow] = lse_v;
+          }
+        }
+        reinterpret_cast<float*>(smem + S_FIN)[r] = live ? 1.f / l_tot : 0.f;
+        fence_proxy_async_smem();
+      }
+      if (!all_ok) failed = true;
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (tid == 64 && all_ok)
+        bulk_copy_to_peer(map_peer(sbase + O_FIN, rank + 2), sbase + S_FIN, kFinBytes,
+                          map_peer(bar(B_FIN_FULL), rank + 2));
+    }
+  } else {
+    // ========================= O-CTAs =========================
+    if (warp == 0) {
+      int u = 0;
+      if (lane == 0) {  // this CTA's 256 value dims of block msg_block(u), one request
+        prefetch_tmap(&tm_v);
+        for (; u < n_msgs; ++u) {
+          const int stage = u % kStagesV;
+          if (u >= kStagesV &&
+              !mbar_wait_cluster(bar(B_HALF_EMPTY + stage), ((u / kStagesV) - 1) & 1)) {
+            failed = true;
+            break;
+          }
+          const uint32_t dst = sbase + O_RING + stage * kTileV;
+          const int krow = (int)block_row(msg_block(u));
+          mbar_expect_tx(bar(B_HALF_FULL + stage), kTileV);
+          tma_load_4d(dst, &tm_v, 0, krow, 2 * half, 0, bar(B_HALF_FULL + stage));
+        }
+        // nothing may land after the CTAs leave (and the last block is zeroed below)
+        for (int v = max(0, u - kStagesV); v < u; ++v)
+          if (!mbar_wait(bar(B_HALF_FULL + v % kStagesV), (v / kStagesV) & 1)) failed = true;
+      }
+      // keys past the end of the sequence in the last block: their values are
+      // zeroed so that 0 * (whatever the page holds) cannot turn into NaN
+      if (__shfl_sync(0xffffffffu, (!failed && u == n_msgs) ? 1 : 0, 0)) {
+        const long long t0 = (long long)msg_block(n_msgs - 1) * kBK;
+        if (t0 + kBK > n_keys) {
+          unsigned char* base = smem + O_RING + ((n_msgs - 1) % kStagesV) * kTileV;
+          const int r0 = (int)(n_keys - t0);
+          for (int e = lane; e < (kBK - r0) * 32; e += 32) {  // 16-byte units, 4 chunks
+            const int rr = r0 + (e >> 5), c = (e >> 3) & 3, q = e & 7;
+            reinterpret_cast<uint4*>(base + c * kVChunk + (rr >> 3) * 1024 + (rr & 7) * 128)[q] =
+                make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (rank == 2) mbar_arrive(bar(B_TAIL_OK));
+          else mbar_arrive_cluster(map_peer(bar(B_TAIL_OK), 2));
+        }
+      }
+    } else if (warp == 1 && rank == 2) {
+      if (lane == 0) {  // PV for both O-CTAs: A = P (K-major), B = value halves (MN-major)
+        // Before PV of message jj the O rows of a quadrant whose flag is set in
+        // the message are multiplied by the row's factor; this thread reads the
+        // flags of both CTAs' messages and calls the row warps only then.
+        const uint32_t msg3 = map_peer(sbase + O_MSG, 3);
+        const uint32_t go3 = map_peer(bar(B_GO), 3);
+        const uint32_t goidx3 = map_peer(sbase + O_GO, 3);
+        uint32_t n_go2 = 0, n_go3 = 0;  // completed rescale calls per CTA
+        for (int jj = 0; jj < n_msgs && !failed; ++jj) {
+          const int mb = jj % kMsgSlots;
+          const uint32_t ph = (jj / kMsgSlots) & 1;
+          const int stage = jj % kStagesV;
+          if (!mbar_wait(bar(B_P_FULL + mb), ph) || !mbar_wait_cluster(bar(B_P_PEER + mb), ph)) {
+            failed = true;
+            break;
+          }
+          if (jj > 0) {
+            const uint4 f2 =
+                *reinterpret_cast<const uint4*>(smem + O_MSG + mb * kMsgStride + kPBytes + kHM * 4);
+            const uint4 f3 = ld_cluster_v4(msg3 + mb * kMsgStride + kPBytes + kHM * 4);
+            const bool r2 = (f2.x | f2.y | f2.z | f2.w) != 0;
+            const bool r3 = (f3.x | f3.y | f3.z | f3.w) != 0;
+            if (r2 || r3) {
+              // O is rescaled once PV of the previous message has completed
+              if (!mbar_wait(bar(B_PV_DONE + (jj - 1) % kMsgSlots), ((jj - 1) / kMsgSlots) & 1)) {
+                failed = true;
+                break;
+              }
+              if (r2) {
+                *reinterpret_cast<volatile int32_t*>(smem + O_GO) = jj;
+                mbar_arrive(bar(B_GO));
+              }
+              if (r3) {
+                st_cluster_u32(goidx3, (uint32_t)jj);
+                mbar_arrive_cluster(go3);
+              }
+              if ((r2 && !mbar_wait(bar(B_O_READY + 0), n_go2++ & 1)) ||
+                  (r3 && !mbar_wait_cluster(bar(B_O_READY + 1), n_go3++ & 1))) {
+                failed = true;
+                break;
+              }
+            }
+          }
+          if (!mbar_wait(bar(B_HALF_FULL + stage), (jj / kStagesV) & 1) ||
+              !mbar_wait_cluster(bar(B_HALF_PEER + stage), (jj / kStagesV) & 1) ||
+              (jj == n_msgs - 1 && !mbar_wait_cluster(bar(B_TAIL_OK), 0))) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t pa = sbase + O_MSG + mb * kMsgStride;
+          const uint32_t h0 = sbase + O_RING + stage * kTileV;
+          const uint32_t h1 = h0 + 2 * kVChunk;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t ad = smem_desc(pa + kk * 32, 16, 1024, kSwizzle128B);
+            const uint32_t acc = (jj > 0 || kk > 0) ? 1u : 0u;
+            umma_pair_bf16(tmem, ad, smem_desc(h0 + kk * 2048, kVChunk, 1024, kSwizzle128B),
+                           kIdescPV, acc);
+            umma_pair_bf16(tmem + 256, ad,
+                           smem_desc(h1 + kk * 2048, kVChunk, 1024, kSwizzle128B), kIdescPV, acc);
+          }
+          umma_pair_commit(bar(B_PV_DONE + mb), kMaskO);
+          umma_pair_commit(bar(B_HALF_EMPTY + stage), kMaskO);
+          umma_pair_commit(bar(B_P_FREE + mb), kMaskS);
+        }
+        umma_pair_commit(bar(B_MMA_DONE), 0x4);
+        if (!mbar_wait(bar(B_MMA_DONE), 0)) failed = true;
+        // the row warps of both CTAs leave their loop (even after a failure)
+        *reinterpret_cast<volatile int32_t*>(smem + O_GO) = -1;
+        mbar_arrive(bar(B_GO));
+        st_cluster_u32(goidx3, 0xffffffffu);
+        mbar_arrive_cluster(go3);
+      }
+    } else if (rank == 3 && warp == 8) {
+      // relay: this CTA's value half of block u has landed -> rank 2's PV issuer
+      if (lane == 0) {
+        const uint32_t peer2 = map_peer(bar(B_HALF_PEER), 2);
+        for (int u = 0; u < n_msgs; ++u) {
+          if (!mbar_wait(bar(B_HALF_FULL + u % kStagesV), (u / kStagesV) & 1)) {
+            failed = true;
+            break;
+          }
+          mbar_arrive_cluster(peer2 + 8 * (u % kStagesV));
+        }
+      }
+    } else if (warp == 7) {
+      // ---------------- relay: incoming messages --------------------------------
+      // Once a message has landed here: arm its slot for the message after
+      // next-but-two, free the S-CTA's staging slot it came from, and (rank 3)
+      // tell rank 2's PV issuer.
+      if (lane == 0) {
+        const uint32_t stage_free0 = map_peer(bar(B_STAGE_FREE), rank - 2);
+        const uint32_t ppeer2 = map_peer(bar(B_P_PEER), 2);
+        for (int jj = 0; jj < n_msgs; ++jj) {
+          const int mb = jj % kMsgSlots;
+          if (!mbar_wait_cluster(bar(B_P_FULL + mb), (jj / kMsgSlots) & 1)) {
+            failed = true;
+            break;
+          }
+          if (jj + kMsgSlots < n_msgs) mbar_expect_tx(bar(B_P_FULL + mb), kMsgBytes);
+          mbar_arrive_cluster(stage_free0 + 8 * (jj % kStageSlots));
+          if (rank == 3) mbar_arrive_cluster(ppeer2 + 8 * mb);
+        }
+      }
+    } else if (warp >= 2 && warp <= 5) {
+      // ---------------- row warps: rescales when called, output ---------------
+      const int qd = warp & 3;
+      const int r = qd * 32 + lane;
+      const uint32_t t_lane = tmem + ((uint32_t)(qd * 32) << 16);
+      const int lr = rt * kTM + half * kHM + r;
+      const bool row_ok = lr < QH;
+      const uint32_t oready = rank == 2 ? bar(B_O_READY + 0) : map_peer(bar(B_O_READY + 1), 2);
+      // Each GO call names a message whose flags ask for a rescale (PV of the
+      // message before it has completed), or -1 at the end. Bounded: there are
+      // at most n_msgs calls plus the last.
+      for (int call = 0; call <= n_msgs; ++call) {
+        if (!__all_sync(0xffffffffu, mbar_wait_cluster(bar(B_GO), call & 1))) {
+          failed = true;
+          break;
+        }
+        const int jj = *reinterpret_cast<volatile const int32_t*>(smem + O_GO);
+        if (jj < 0) break;
+        const int mb = jj % kMsgSlots;
+        const unsigned char* msg = smem + O_MSG + mb * kMsgStride;
+        const uint4 fl = *reinterpret_cast<const uint4*>(msg + kPBytes + kHM * 4);
+        const uint32_t mine = qd == 0 ? fl.x : qd == 1 ? fl.y : qd == 2 ? fl.z : fl.w;
+        if (mine) {
+          const float f = reinterpret_cast<const float*>(msg + kPBytes)[r];
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < 16; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(t_lane + 32 * c, ov);
+            tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * f);
+            tmem_st32(t_lane + 32 * c, ov);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (rank == 2) mbar_arrive(oready);
+          else mbar_arrive_cluster(oready);
+        }
+      }
+      // ---- epilogue: O / l ---------------------------------------------------
+      if (!__all_sync(0xffffffffu,
+                      !failed && mbar_wait_cluster(bar(B_FIN_FULL), 0) &&
+                          mbar_wait_cluster(bar(B_PV_DONE + (n_msgs - 1) % kMsgSlots),
+                                            ((n_msgs - 1) / kMsgSlots) & 1)))
+        failed = true;
+      if (!failed) {
+        tc_fence_after();
+        const float inv_l = reinterpret_cast<const float*>(smem + O_FIN)[r];
+        const long long grow = row0 + r;
+        unsigned char* stage = smem + O_RING + r * kOutStride;
+        const uint32_t stage_s = sbase + O_RING + r * kOutStride;
+#pragma unroll 1
+        for (int c = 0; c < 16; c += 2) {
+          uint32_t ov[2][32];
+          tmem_ld32(t_lane + 32 * c, ov[0]);
+          tmem_ld32(t_lane + 32 * (c + 1), ov[1]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint4* dst = reinterpret_cast<uint4*>(stage + (c + h) * 64);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(pack_bf16(__uint_as_float(ov[h][8 * q + 0]) * inv_l,
+                                            __uint_as_float(ov[h][8 * q + 1]) * inv_l),
+                                  pack_bf16(__uint_as_float(ov[h][8 * q + 2]) * inv_l,
+                                            __uint_as_float(ov[h][8 * q + 3]) * inv_l),
+                                  pack_bf16(__uint_as_float(ov[h][8 * q + 4]) * inv_l,
+                                            __uint_as_float(ov[h][8 * q + 5]) * inv_l),
+                                  pack_bf16(__uint_as_float(ov[h][8 * q + 6]) * inv_l,
+                                            __uint_as_float(ov[h][8 * q + 7]) * inv_l));
+          }
+        }
+        fence_proxy_async_smem();
+        if (row_ok)
+          bulk_s2g(p.n_split == 1 ? p.out + grow * kC
+                                  : p.part_o + ((long long)sp * total_rows + grow) * kC,
+                   stage_s, 1024);
+        bulk_commit();
+        bulk_wait0();
+      }
+    } else if (warp == 6 && rank == 2) {
+      // ---------------- the fused tree build --------------------------------
+      if (builds) {
+        bool bad = false;
+        const int n = fused_build(p.tf, b, smem + O_BUILD, &bad);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t src = sbase + O_BUILD + (uint32_t)offsetof(tb::Smem, anc);
+          for (uint32_t s = 0; s < 2; ++s)
+            bulk_copy_to_peer(map_peer(sbase + S_VIS, s), src, vis_bytes,
+                              map_peer(bar(B_TREE), s));
+        }
+        if (designated) fused_write(p, b, smem + O_BUILD, n, bad);
+      }
+    }
+  }
+
+  // the ancestor words have landed before the S-CTAs leave
+  if (builds && s_side && tid == 0 && !mbar_wait_cluster(bar(B_TREE), 0)) failed = true;
+  if (failed) atomicOr(p.status + b, DDT_ST_TIMEOUT);
+  __syncthreads();
+  cluster_sync();  // every pair MMA, copy and remote arrive of the cluster has completed
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, kTmemCols);
+  }
+  cluster_sync();
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// Keys: the cache as {64 dims, rows, 9 chunks} (strides: row, 128 B); a box of
+// {64, 64, 9} lands as nine 64-key x 128-byte swizzled chunks (8 KB each).
+// Values: the c_kv part as {64 dims, rows, 4 chunks, 2 halves} (strides: row,
+// 128 B, 512 B); a box of {64, 64, 2, 2} at chunk 2h holds dims
+// [128h, 128h + 128) and [256 + 128h, 256 + 128h + 128) as four 8 KB chunks.
+// Queries: as in the 128-row kernel, 128 rows per box.
+bool encode_maps(CUtensorMap* mk, CUtensorMap* mv, CUtensorMap* ml, CUtensorMap* mp,
+                 const void* kv, uint64_t kv_rows, const void* q_lat, const void* q_pe,
+                 uint64_t q_rows) {
+  auto fn = encoder();
+  if (fn == nullptr) return false;
+  const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  const auto l2 = CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
+  const auto oob = CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE;
+  const auto il = CU_TENSOR_MAP_INTERLEAVE_NONE;
+  const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  cuuint32_t e4[4] = {1, 1, 1, 1};
+  {
+    cuuint64_t dims[3] = {64, kv_rows, (cuuint64_t)kChunks};
+    cuuint64_t str[2] = {(cuuint64_t)(kC + kR) * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)kBK, (cuuint32_t)kChunks};
+    if (fn(mk, bf, 3, const_cast<void*>(kv), dims, str, box, e4, il, sw, l2, oob) != CUDA_SUCCESS)
+      return false;
+  }
+  {
+    cuuint64_t dims[4] = {64, kv_rows, 4, 2};
+    cuuint64_t str[3] = {(cuuint64_t)(kC + kR) * 2, 128, 512};
+    cuuint32_t box[4] = {64, (cuuint32_t)kBK, 2, 2};
+    if (fn(mv, bf, 4, const_cast<void*>(kv), dims, str, box, e4, il, sw, l2, oob) != CUDA_SUCCESS)
+      return false;
+  }
+  {
+    cuuint64_t dims[3] = {64, q_rows, (cuuint64_t)(kC / 64)};
+    cuuint64_t str[2] = {(cuuint64_t)kC * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)kHM, (cuuint32_t)(kC / 64)};
+    if (fn(ml, bf, 3, const_cast<void*>(q_lat), dims, str, box, e4, il, sw, l2, oob) !=
+        CUDA_SUCCESS)
+      return false;
+  }
+  cuuint64_t dp[2] = {64, q_rows};
+  cuuint64_t spe[1] = {(cuuint64_t)kR * 2};
+  cuuint32_t bp[2] = {64, (cuuint32_t)kHM};
+  return fn(mp, bf, 2, const_cast<void*>(q_pe), dp, spe, bp, e4, il, sw, l2, oob) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int verify_attn_pair_clusters_per_wave() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] != 0) return cached[dev];
+  static int smem_set[64] = {};
+  if (ensure_smem_limit(k_verify_attn_pair, (int)kSmemBytes, smem_set) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(4 * 64, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 4;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k_verify_attn_pair, &cfg) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cached[dev] = n;
+  return n;
+}
+
+cudaError_t launch_verify_attn_pair(const ddt_attn_dims& d, int n_split, const void* q_lat,
+                                    const void* q_pe, const void* kv, const int32_t* block_table,
+                                    const int32_t* prefix_len, const uint64_t* vis_bits, void* out,
+                                    float* lse, int32_t* status, __nv_bfloat16* part_o,
+                                    float* part_lse, cudaStream_t stream, const TreeFuse* fuse) {
+  const long long QH = (long long)d.Q * d.H;
+  const long long rows = (long long)d.B * QH;
+  if (d.kv_rows < 1 || rows > 0x7fffffffLL || d.kv_rows > 0x7fffffffLL || n_split < 1)
+    return cudaErrorInvalidValue;
+  CUtensorMap tm_k, tm_v, tm_ql, tm_qp;
+  if (!encode_maps(&tm_k, &tm_v, &tm_ql, &tm_qp, kv, (uint64_t)d.kv_rows, q_lat, q_pe,
+                   (uint64_t)rows))
+    return cudaErrorInvalidValue;
+  Params p;
+  p.B = d.B; p.Q = d.Q; p.H = d.H;
+  p.page_size = d.page_size; p.max_pages = d.max_pages; p.kv_rows = d.kv_rows;
+  p.scale_log2 = d.scale * 1.4426950408889634f;
+  p.n_rt = (int)((QH + kTM - 1) / kTM);
+  p.n_split = n_split;
+  p.block_table = block_table; p.prefix_len = prefix_len;
+  p.vis_bits = reinterpret_cast<const unsigned long long*>(vis_bits);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse; p.status = status;
+  p.part_o = part_o; p.part_lse = part_lse;
+  p.fuse = fuse != nullptr ? 1 : 0;
+  p.tf = fuse != nullptr ? *fuse : TreeFuse{};
+  static int smem_set[64] = {};
+  cudaError_t e = ensure_smem_limit(k_verify_attn_pair, (int)kSmemBytes, smem_set);
+  if (e != cudaSuccess) return e;
+  const long long units = (long long)d.B * p.n_rt * n_split;
+  k_verify_attn_pair<<<(unsigned)(units * 4), kThreads, kSmemBytes, stream>>>(tm_k, tm_v, tm_ql,
+                                                                              tm_qp, p);
+  return cudaGetLastError();
+}
+
+}  // namespace ddt
