@@ -83,30 +83,39 @@ def measured_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one
-# k_verify_attn_bf16 launch, from ncu captures of the kernel built from the
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
+# the attention kernel the dispatcher picks for a workload (128-row tiles:
+# k_verify_attn_bf16 in verify_attn_bf16.cu; 256-row tiles: k_verify_attn_pair
+# in verify_attn_pair.cu), from ncu captures of the kernel built from the
 # source whose sha256 is given; reported as null once that source changes.
 MEASURED_TRAFFIC = {
-    "c2_max_budget": ("ef00f2f1daac8551449d88589bbf9c567da818205732f9511a776cf3981e3cdf",
-                      9833728),
-    "c3_batched_paged": ("ef00f2f1daac8551449d88589bbf9c567da818205732f9511a776cf3981e3cdf",
-                         502738688 + 61799680),
-    "c4_deep_long": ("ef00f2f1daac8551449d88589bbf9c567da818205732f9511a776cf3981e3cdf",
-                     547618048 + 60359424),
+    ("c2_max_budget", 256): ("verify_attn_pair.cu",
+                             "1faffa2d2bd194e71e8c69231e6afb1e6b6b79b3d0bac158d15a7be7c562e30c",
+                             9950976 + 0),
+    ("c4_deep_long", 256): ("verify_attn_pair.cu",
+                            "1faffa2d2bd194e71e8c69231e6afb1e6b6b79b3d0bac158d15a7be7c562e30c",
+                            884251648 + 38849792),
+    ("c3_batched_paged", 128): ("verify_attn_bf16.cu",
+                                "79b0bd59b655e27bb215965f48b6ac16293cd104f864987f8061f08566f3090d",
+                                502247424 + 62564352),
 }
 
 
-def measured_traffic(w):
+def attn_kernel_name(rows: int) -> str:
+    return "k_verify_attn_pair" if rows == 256 else "k_verify_attn_bf16"
+
+
+def measured_traffic(w, rows: int):
     """ncu DRAM bytes per launch of the attention kernel for workload w, or
     None when none was taken for the current kernel source."""
     import hashlib
-    entry = MEASURED_TRAFFIC.get(w.name)
+    entry = MEASURED_TRAFFIC.get((w.name, rows))
     if entry is None:
         return None
-    src = os.path.join(ROOT, "tree_speculative_decoding_ddt_gb300", "csrc", "verify_attn_bf16.cu")
+    src = os.path.join(ROOT, "tree_speculative_decoding_ddt_gb300", "csrc", entry[0])
     with open(src, "rb") as f:
         digest = hashlib.sha256(f.read()).hexdigest()
-    return entry[1] if digest == entry[0] else None
+    return entry[2] if digest == entry[1] else None
 
 
 def attn_work(w, prefix_len, depths, dtype_bytes):
@@ -315,7 +324,8 @@ def run_ours(args):
     buf.target_argmax.copy_(i32(WL.target_argmax_for(batch, depths)))
     torch.cuda.synchronize()
 
-    split = DB.ddt_verify_attn_workspace_size(buf.attn) > 0
+    split = bf16 and DB.ddt_verify_attn_splits(buf.attn) > 1
+    attn_rows = DB.ddt_verify_attn_rows_per_tile(buf.attn) if bf16 else 0
     # build + attention (fused for bf16 when the candidate table is small), split merge, accept
     fused = w.dtype == "bf16" and min(w.D, w.budget) * min(w.K, w.budget) <= 1024
     launches_per_step = (2 if fused else 3) + (1 if split else 0)
@@ -453,8 +463,9 @@ def run_ours(args):
             "unit": "TFLOP/s" if bound == "tensor" else "GB/s",
             "frac": (achieved_tf / tf) if bound == "tensor" else (achieved_gb / hbm),
             "peak_source": f"{src} (MEASURED_PEAKS.json burst)" if src == "measured" else src,
-            "traffic": measured_traffic(w) if bf16 else None,
-            "traffic_kernel": "k_verify_attn_bf16 (ncu, one launch)",
+            "traffic": measured_traffic(w, attn_rows) if bf16 else None,
+            "traffic_kernel": f"{attn_kernel_name(attn_rows)} (ncu, one launch)",
+            "rows_per_tile": attn_rows, "key_splits": DB.ddt_verify_attn_splits(buf.attn) if bf16 else 1,
             "algorithmic_flops": flops, "algorithmic_bytes": byt,
             "attn_us": attn_s * 1e6, "roofline_us": t_roof * 1e6,
             "frac_of_roofline_time": t_roof / attn_s,

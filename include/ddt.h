@@ -139,6 +139,13 @@ size_t ddt_verify_attn_workspace_size(const ddt_attn_dims* dims);
  * counterpart on the source pages); 0 for invalid or DDT_F32 dims. */
 int ddt_verify_attn_rows_per_tile(const ddt_attn_dims* dims);
 
+/* Number of key ranges each sequence's keys are split into by the DDT_BF16
+ * verify attention for these dims on the current device (1: no split and no
+ * merge pass; >1: partial results in the workspace, merged by a second
+ * kernel). Informational (no counterpart on the source pages); 0 for invalid
+ * or DDT_F32 dims. */
+int ddt_verify_attn_splits(const ddt_attn_dims* dims);
+
 /* B. Tree-verify MLA-absorb attention.
  * "The Checkpoint: Committing a Working Native DDTree Engine", section "The
  * Message" (attention via the custom verify_attn in absorb form; KV-cache

@@ -61,6 +61,7 @@ SIGNATURES = {
     "ddt_tree_build": (ctypes.c_int, [ctypes.POINTER(TreeDims)] + [_P] * 13),
     "ddt_verify_attn_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(AttnDims)]),
     "ddt_verify_attn_rows_per_tile": (ctypes.c_int, [ctypes.POINTER(AttnDims)]),
+    "ddt_verify_attn_splits": (ctypes.c_int, [ctypes.POINTER(AttnDims)]),
     "ddt_verify_attn": (ctypes.c_int, [ctypes.POINTER(AttnDims)] + [_P] * 10 +
                         [ctypes.c_size_t, _P]),
     "ddt_verify_attn_noalloc": (ctypes.c_int, [ctypes.POINTER(AttnDims)] + [_P] * 10),
@@ -161,6 +162,12 @@ def ddt_verify_attn_rows_per_tile(dims: AttnDims) -> int:
     """Query rows per tile (128 or 256) of the bf16 verify attention for these
     dims on the current device; 0 for invalid or fp32 dims."""
     return int(load().ddt_verify_attn_rows_per_tile(ctypes.byref(dims)))
+
+
+def ddt_verify_attn_splits(dims: AttnDims) -> int:
+    """Key ranges per sequence of the bf16 verify attention for these dims on
+    the current device (1 = no merge pass); 0 for invalid or fp32 dims."""
+    return int(load().ddt_verify_attn_splits(ctypes.byref(dims)))
 
 
 def ddt_verify_attn(q_lat, q_pe, kv_cache, block_table, prefix_len, vis_bits, scale: float,

@@ -146,6 +146,11 @@ int ddt_verify_attn_rows_per_tile(const ddt_attn_dims* dims) {
   return ddt::verify_attn_bf16_rows_per_tile(*dims);
 }
 
+int ddt_verify_attn_splits(const ddt_attn_dims* dims) {
+  if (check_attn_dims(dims) != DDT_OK || dims->dtype != DDT_BF16) return 0;
+  return ddt::verify_attn_bf16_splits(*dims);
+}
+
 int ddt_verify_attn(const ddt_attn_dims* dims, const void* q_lat, const void* q_pe,
                     const void* kv_cache, const int32_t* block_table, const int32_t* prefix_len,
                     const uint64_t* vis_bits, void* out, float* lse, int32_t* status,

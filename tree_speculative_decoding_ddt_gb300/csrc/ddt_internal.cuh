@@ -91,8 +91,10 @@ cudaError_t launch_verify_attn_pair(const ddt_attn_dims& d, int n_split, const v
                                     const int32_t* prefix_len, const uint64_t* vis_bits, void* out,
                                     float* lse, int32_t* status, __nv_bfloat16* part_o,
                                     float* part_lse, cudaStream_t stream, const TreeFuse* fuse);
-// Row-tile height (128 or 256) the next bf16 launch with these dims uses.
+// Row-tile height (128 or 256) and key-range split the next bf16 launch with
+// these dims uses.
 int verify_attn_bf16_rows_per_tile(const ddt_attn_dims& d);
+int verify_attn_bf16_splits(const ddt_attn_dims& d);
 
 // Host checks of a verify-attention call (defined in ddt_api.cu).
 int check_verify_attn_args(const ddt_attn_dims* d, const void* q_lat, const void* q_pe,

@@ -1133,5 +1133,6 @@ cudaError_t launch_verify_attn_bf16(const ddt_attn_dims& d, const void* q_lat, c
 }
 
 int verify_attn_bf16_rows_per_tile(const ddt_attn_dims& d) { return choose_plan(d).rows; }
+int verify_attn_bf16_splits(const ddt_attn_dims& d) { return choose_plan(d).n_split; }
 
 }  // namespace ddt
