@@ -7,6 +7,8 @@ step, written for checking the CUDA path and never called by it:
 * :func:`verify_attention` tree-verify MLA-absorb attention in float64
 * :func:`tree_accept`      greedy walk from the root, bonus token
 * :func:`cache_compact`    gather of the accepted-path latents
+* :func:`target_argmax`    the target's greedy token at every tree slot (the
+                           input of tree_accept, one step upstream)
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this module. It shares no code with the CUDA path:
@@ -369,6 +371,21 @@ def ddt_step(topk_logp, topk_ids, root_tok, budget: int, V: int, q_lat, q_pe, kv
     status = tree["status"] | attn_status | acc["status"] | cst
     return dict(tree=tree, o=o, lse=lse, target=target, accept=acc, kv=new_kv,
                 new_len=new_len, status=status)
+
+
+# ================================================ next: target-side argmax
+
+def target_argmax(logits) -> np.ndarray:
+    """The target model's greedy token at every tree slot: the index of the
+    largest logit over the vocabulary (last axis). "The Checkpoint: Committing a
+    Working Native DDTree Engine", "The Message": the target's argmax at each
+    tree node is what tree_accept compares the drafted tokens with.
+
+    Ties go to the lowest index; -0.0 equals +0.0; a NaN counts as larger than
+    every number (the first NaN wins), as numpy's argmax treats it.
+    """
+    x = np.asarray(logits, dtype=np.float64)
+    return np.argmax(x, axis=-1).astype(np.int32)
 
 
 # =================================================== multi-step decode (loop)

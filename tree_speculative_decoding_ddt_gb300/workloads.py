@@ -40,6 +40,8 @@ STREAM_LATENT = 1
 STREAM_TARGET = 2
 STREAM_BATCH = 3
 STREAM_ROOT = 4
+STREAM_TARGET_LOGITS = 5
+STREAM_DRAFTER_LOGITS = 6
 
 #: rows of the latent cache generated per random-number call (keeps peak host
 #: memory bounded and lets any row block be regenerated on its own)
@@ -298,6 +300,19 @@ def synth_target_argmax(depths: np.ndarray, topk_ids: np.ndarray, u: np.ndarray,
     ok = (d >= 0) & (d < D) & (np.asarray(u) < p)
     out[ok] = topk_ids[d[ok], 0]
     return out
+
+
+def target_logits(w: Workload, b: int, winners: Optional[np.ndarray] = None) -> np.ndarray:
+    """Synthetic target logits [Q, V] of sequence ``b``: N(0, ``logit_std``)
+    (bf16-rounded on bf16 workloads). With ``winners`` (a token per slot) that
+    token's logit is raised one unit above the slot's largest, so the slot's
+    greedy token is the given one."""
+    g = rng(w.cid, b, STREAM_TARGET_LOGITS)
+    x = g.normal(0.0, w.logit_std, (w.Q, w.V))
+    if winners is not None:
+        x[np.arange(w.Q), np.asarray(winners)] = x.max(axis=1) + 1.0
+    x = x.astype(np.float32)
+    return round_bf16(x) if w.dtype == "bf16" else x
 
 
 # ---------------------------------------------------------------------- batches
