@@ -280,6 +280,41 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ GPU arm
 
+def time_next_rows(w, dev, stream, flush, n: int) -> dict:
+    """Event-timed launches of the steps next to the verify step on this
+    workload's shapes (L2 flushed before each launch), each against the HBM
+    roofline of its algorithmic bytes: the target-side argmax over
+    B*Q x V logits."""
+    import torch
+    from tree_speculative_decoding_ddt_gb300 import _binding as DB
+    hbm, _, src = measured_peaks()
+    out = {}
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234)
+    ldt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    logits = (torch.randn((w.B * w.Q, w.V), generator=gen, device=dev) * w.logit_std).to(ldt)
+    am = torch.empty((w.B * w.Q,), dtype=torch.int32, device=dev)
+    DB.ddt_target_argmax(logits, out=am)
+    ts = []
+    for _ in range(max(5, min(n, 50))):
+        flush.fill_(1)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        DB.ddt_target_argmax(logits, out=am)
+        e.record(stream)
+        ts.append((s, e))
+    torch.cuda.synchronize()
+    sec = statistics.median([s.elapsed_time(e) for s, e in ts]) / 1e3
+    byt = logits.numel() * logits.element_size() + am.numel() * 4
+    out["target_argmax"] = {"kernel": "k_target_argmax", "rows": w.B * w.Q, "V": w.V,
+                            "us": sec * 1e6, "bound": "hbm", "achieved": byt / sec / 1e9,
+                            "peak": hbm, "unit": "GB/s", "frac": byt / sec / 1e9 / hbm,
+                            "algorithmic_bytes": byt, "peak_source": src,
+                            "data": "seeded device normal logits"}
+    del logits
+    return out
+
+
 def run_ours(args):
     import torch
     from tree_speculative_decoding_ddt_gb300 import _binding as DB
@@ -382,6 +417,8 @@ def run_ours(args):
         aevs = timed(run["attn"], n_attn)
         torch.cuda.synchronize()
         attn_ms = [s.elapsed_time(e) for s, e in aevs]
+        # the next rows of the path, on this workload's shapes, timed the same way
+        next_rows = time_next_rows(w, dev, stream, flush, n_attn)
     clocks = clk.summary()
 
     # end to end through the public API: host inputs in pinned memory are
@@ -476,6 +513,7 @@ def run_ours(args):
                 "unit": "steps/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms)},
+        "next": next_rows,
     }
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
         n_cpu = max(1, int(args.cpu_seconds // 2))

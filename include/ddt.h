@@ -287,6 +287,25 @@ size_t ddt_step_workspace_size(const ddt_step_args* args);
  * overwritten, then OR-ed by every stage. */
 int ddt_step(const ddt_step_args* args, cudaStream_t stream);
 
+/* Target-side argmax at every tree slot: the target model's greedy token,
+ * the input tree_accept compares the drafted tokens with.
+ * "The Checkpoint: Committing a Working Native DDTree Engine", section "The
+ * Message" (the target's argmax at each tree node feeds tree_accept).
+ *
+ * logits: rows x V values, row-major (rows = B * Q tree slots, in the slot
+ * order of the tree arrays), dtype DDT_BF16 or DDT_F32, caller-owned device
+ * memory. argmax: int32 [rows], caller-owned device memory, written with the
+ * index of each row's largest logit: ties go to the lowest index, -0.0 equals
+ * +0.0, a NaN counts as larger than every number (the first NaN wins).
+ * Rows that start on a 16-byte boundary with V a multiple of 8 (bf16) or 4
+ * (f32) are read with vector loads, others element by element; any V >= 1 is
+ * accepted. Limits: 1 <= rows <= 2^28 - 1, 1 <= V <= 2^31 - 1. Returns
+ * DDT_EINVAL for a null pointer, a size below 1 or an unknown dtype,
+ * DDT_EUNSUPPORTED past the limits. Enqueues one kernel on `stream`;
+ * allocates nothing. */
+int ddt_target_argmax(int64_t rows, int64_t V, int dtype, const void* logits, int32_t* argmax,
+                      cudaStream_t stream);
+
 /* Static text for a DDT_E* return code. */
 const char* ddt_strerror(int code);
 

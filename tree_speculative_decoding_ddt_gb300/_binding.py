@@ -69,6 +69,8 @@ SIGNATURES = {
     "ddt_cache_compact": (ctypes.c_int, [ctypes.c_int32] * 5 + [ctypes.c_int64] + [_P] * 8),
     "ddt_step_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(StepArgs)]),
     "ddt_step": (ctypes.c_int, [ctypes.POINTER(StepArgs), _P]),
+    "ddt_target_argmax": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int, _P, _P,
+                                         _P]),
     "ddt_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "ddt_abi_version": (ctypes.c_int, []),
 }
@@ -263,6 +265,29 @@ def ddt_tree_accept(tokens, parents, target_argmax, D: int, status=None, stream=
                                 _stream(stream))
     _check("ddt_tree_accept", rc)
     return o
+
+
+def ddt_target_argmax(logits: torch.Tensor, out: Optional[torch.Tensor] = None,
+                      stream=None) -> torch.Tensor:
+    """Greedy token at every tree slot: int32 argmax over the last axis of
+    ``logits`` (bf16 or f32, contiguous, any leading shape)."""
+    if not isinstance(logits, torch.Tensor) or not logits.is_cuda:
+        raise TypeError("logits must be a CUDA tensor")
+    if logits.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError(f"logits must be bfloat16 or float32, got {logits.dtype}")
+    if not logits.is_contiguous():
+        raise ValueError("logits must be contiguous")
+    V = int(logits.shape[-1])
+    lead = tuple(logits.shape[:-1])
+    rows = int(logits.numel() // max(V, 1))
+    if out is None:
+        out = torch.empty(lead, dtype=torch.int32, device=logits.device)
+    else:
+        _need(out, "out", torch.int32, lead)
+    dt = DDT_BF16 if logits.dtype == torch.bfloat16 else DDT_F32
+    rc = load().ddt_target_argmax(rows, V, dt, _ptr(logits), _ptr(out), _stream(stream))
+    _check("ddt_target_argmax", rc)
+    return out
 
 
 def ddt_cache_compact(kv_cache, block_table, prefix_len, accept_idx, accept_len, page_size: int,

@@ -203,6 +203,14 @@ int ddt_cache_compact(int32_t B, int32_t D, int32_t row_bytes, int32_t page_size
   return launched(ddt::launch_accept_compact(a, stream));
 }
 
+int ddt_target_argmax(int64_t rows, int64_t V, int dtype, const void* logits, int32_t* argmax,
+                      cudaStream_t stream) {
+  if (!logits || !argmax || rows < 1 || V < 1) return DDT_EINVAL;
+  if (dtype != DDT_BF16 && dtype != DDT_F32) return DDT_EINVAL;
+  if (rows > (int64_t(1) << 28) - 1 || V > 0x7fffffffLL) return DDT_EUNSUPPORTED;
+  return launched(ddt::launch_target_argmax(rows, V, dtype, logits, argmax, stream));
+}
+
 size_t ddt_step_workspace_size(const ddt_step_args* args) {
   if (args == nullptr) return 0;
   return ddt_verify_attn_workspace_size(&args->attn);

@@ -96,6 +96,10 @@ cudaError_t launch_verify_attn_pair(const ddt_attn_dims& d, int n_split, const v
 int verify_attn_bf16_rows_per_tile(const ddt_attn_dims& d);
 int verify_attn_bf16_splits(const ddt_attn_dims& d);
 
+// Target-side argmax over the vocabulary, one row per tree slot.
+cudaError_t launch_target_argmax(long long rows, long long V, int dtype, const void* logits,
+                                 int32_t* argmax, cudaStream_t stream);
+
 // Host checks of a verify-attention call (defined in ddt_api.cu).
 int check_verify_attn_args(const ddt_attn_dims* d, const void* q_lat, const void* q_pe,
                            const void* kv, const int32_t* block_table, const int32_t* prefix_len,
