@@ -9,6 +9,8 @@ step, written for checking the CUDA path and never called by it:
 * :func:`cache_compact`    gather of the accepted-path latents
 * :func:`target_argmax`    the target's greedy token at every tree slot (the
                            input of tree_accept, one step upstream)
+* :func:`drafter_topk`     the drafter's per-depth top-K log-probs (the input
+                           of tree_build, one step upstream)
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this module. It shares no code with the CUDA path:
@@ -386,6 +388,40 @@ def target_argmax(logits) -> np.ndarray:
     """
     x = np.asarray(logits, dtype=np.float64)
     return np.argmax(x, axis=-1).astype(np.int32)
+
+
+# ============================================ next: drafter log-softmax top-K
+
+def drafter_topk(logits, K: int):
+    """Per-depth top-K candidates of the drafter from its logits (last axis
+    = vocabulary): the K largest logits, ranked by value (descending) then by
+    token id (ascending), and their log-probabilities
+    ``logit - log(sum(exp(logits)))``. The tree builder's input: "The
+    Milestone Commit: Cementing a Native DDTree Inference Engine", "What the
+    Message Actually Does" (the GPU tree builder consumes per-depth top-K
+    log-probs), and the verify-step specification (node score = sum of the
+    log-probs along the path).
+
+    The ranking uses the logits exactly as given; the log-sum-exp is taken in
+    float64 (shifted by the row maximum) and the log-probs are handed over as
+    float32, as the builder takes them. Returns (logp f32 [..., K],
+    ids int32 [..., K]).
+    """
+    x = np.asarray(logits, dtype=np.float64)
+    lead = x.shape[:-1]
+    V = x.shape[-1]
+    flat = x.reshape(-1, V)
+    logp = np.zeros((flat.shape[0], K), np.float32)
+    ids = np.zeros((flat.shape[0], K), np.int32)
+    cols = np.arange(V)
+    for r in range(flat.shape[0]):
+        row = flat[r]
+        order = np.lexsort((cols, -row))[:K]   # value descending, id ascending
+        m = row.max()
+        lse = m + math.log(float(np.exp(row - m).sum()))
+        ids[r] = order.astype(np.int32)
+        logp[r] = (row[order] - lse).astype(np.float32)
+    return logp.reshape(lead + (K,)), ids.reshape(lead + (K,))
 
 
 # =================================================== multi-step decode (loop)

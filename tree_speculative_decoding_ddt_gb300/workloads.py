@@ -315,6 +315,18 @@ def target_logits(w: Workload, b: int, winners: Optional[np.ndarray] = None) -> 
     return round_bf16(x) if w.dtype == "bf16" else x
 
 
+def drafter_logits(w: Workload, b: int) -> np.ndarray:
+    """Synthetic drafter logits [D, V] of sequence ``b``: N(0, ``logit_std``)
+    with ``boost_rank0`` added to each row's largest entry (bf16-rounded on
+    bf16 workloads)."""
+    g = rng(w.cid, b, STREAM_DRAFTER_LOGITS)
+    x = g.normal(0.0, w.logit_std, (w.D, w.V))
+    if w.boost_rank0:
+        x[np.arange(w.D), np.argmax(x, axis=1)] += w.boost_rank0
+    x = x.astype(np.float32)
+    return round_bf16(x) if w.dtype == "bf16" else x
+
+
 # ---------------------------------------------------------------------- batches
 
 @dataclasses.dataclass
