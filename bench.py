@@ -284,7 +284,7 @@ def time_next_rows(w, dev, stream, flush, n: int) -> dict:
     """Event-timed launches of the steps next to the verify step on this
     workload's shapes (L2 flushed before each launch), each against the HBM
     roofline of its algorithmic bytes: the target-side argmax over
-    B*Q x V logits."""
+    B*Q x V logits and the drafter's top-K over B*D x V logits."""
     import torch
     from tree_speculative_decoding_ddt_gb300 import _binding as DB
     hbm, _, src = measured_peaks()
@@ -312,6 +312,26 @@ def time_next_rows(w, dev, stream, flush, n: int) -> dict:
                             "algorithmic_bytes": byt, "peak_source": src,
                             "data": "seeded device normal logits"}
     del logits
+    # the drafter's per-depth top-K over B*D x V logits
+    dl = (torch.randn((w.B * w.D, w.V), generator=gen, device=dev) * w.logit_std).to(ldt)
+    tk = DB.ddt_drafter_topk(dl, w.K)
+    ts = []
+    for _ in range(max(5, min(n, 50))):
+        flush.fill_(1)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        DB.ddt_drafter_topk(dl, w.K, out=tk)
+        e.record(stream)
+        ts.append((s, e))
+    torch.cuda.synchronize()
+    sec = statistics.median([s.elapsed_time(e) for s, e in ts]) / 1e3
+    byt = dl.numel() * dl.element_size() + w.B * w.D * w.K * 8
+    out["drafter_topk"] = {"kernel": "k_drafter_topk", "rows": w.B * w.D, "V": w.V, "K": w.K,
+                           "us": sec * 1e6, "bound": "hbm", "achieved": byt / sec / 1e9,
+                           "peak": hbm, "unit": "GB/s", "frac": byt / sec / 1e9 / hbm,
+                           "algorithmic_bytes": byt, "peak_source": src,
+                           "data": "seeded device normal logits"}
+    del dl
     return out
 
 

@@ -306,6 +306,28 @@ int ddt_step(const ddt_step_args* args, cudaStream_t stream);
 int ddt_target_argmax(int64_t rows, int64_t V, int dtype, const void* logits, int32_t* argmax,
                       cudaStream_t stream);
 
+/* Drafter-side per-depth top-K: the K largest logits of every row and their
+ * log-probabilities, the input of ddt_tree_build.
+ * "The Milestone Commit: Cementing a Native DDTree Inference Engine",
+ * section "What the Message Actually Does" (the GPU tree builder consumes the
+ * drafter's per-depth top-K log-probs); node score = sum of log-probs along
+ * the path.
+ *
+ * logits: rows x V values, row-major (rows = B * D: sequence, then depth),
+ * DDT_BF16 or DDT_F32, caller-owned device memory; finite values and -inf
+ * (at least one finite value per row). topk_logp: float [rows, K],
+ * topk_ids: int32 [rows, K], caller-owned device memory, written rank 0
+ * first: the K largest logits by value (descending), ties to the lower token
+ * id, with log-prob = logit - log(sum over the row of exp(logit)), computed
+ * in fp32 (an online log-sum-exp; within 1e-5 of the exact value at
+ * V = 163840). Rows read with vector loads when 16-byte aligned with V a
+ * multiple of 8 (bf16) or 4 (f32). Limits: 1 <= K <= 16, K <= V,
+ * 1 <= rows <= 2^28 - 1, V <= 2^31 - 1. Returns DDT_EINVAL for a null
+ * pointer, a size below 1 or an unknown dtype, DDT_EUNSUPPORTED past the
+ * limits. Enqueues one kernel; allocates nothing. */
+int ddt_drafter_topk(int64_t rows, int64_t V, int32_t K, int dtype, const void* logits,
+                     float* topk_logp, int32_t* topk_ids, cudaStream_t stream);
+
 /* Static text for a DDT_E* return code. */
 const char* ddt_strerror(int code);
 

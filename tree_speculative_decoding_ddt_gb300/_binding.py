@@ -71,6 +71,8 @@ SIGNATURES = {
     "ddt_step": (ctypes.c_int, [ctypes.POINTER(StepArgs), _P]),
     "ddt_target_argmax": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int, _P, _P,
                                          _P]),
+    "ddt_drafter_topk": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                        ctypes.c_int, _P, _P, _P, _P]),
     "ddt_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "ddt_abi_version": (ctypes.c_int, []),
 }
@@ -288,6 +290,33 @@ def ddt_target_argmax(logits: torch.Tensor, out: Optional[torch.Tensor] = None,
     rc = load().ddt_target_argmax(rows, V, dt, _ptr(logits), _ptr(out), _stream(stream))
     _check("ddt_target_argmax", rc)
     return out
+
+
+def ddt_drafter_topk(logits: torch.Tensor, K: int, out: Optional[dict] = None,
+                     stream=None) -> dict:
+    """Per-depth top-K of the drafter: logits (bf16 or f32, contiguous,
+    [..., V]) -> topk_logp float32 [..., K] and topk_ids int32 [..., K] (the
+    tree builder's inputs)."""
+    if not isinstance(logits, torch.Tensor) or not logits.is_cuda:
+        raise TypeError("logits must be a CUDA tensor")
+    if logits.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError(f"logits must be bfloat16 or float32, got {logits.dtype}")
+    if not logits.is_contiguous():
+        raise ValueError("logits must be contiguous")
+    V = int(logits.shape[-1])
+    lead = tuple(logits.shape[:-1])
+    rows = int(logits.numel() // max(V, 1))
+    dev = logits.device
+    o = out if out is not None else dict(
+        topk_logp=torch.empty(lead + (K,), dtype=torch.float32, device=dev),
+        topk_ids=torch.empty(lead + (K,), dtype=torch.int32, device=dev))
+    _need(o["topk_logp"], "topk_logp", torch.float32, lead + (K,))
+    _need(o["topk_ids"], "topk_ids", torch.int32, lead + (K,))
+    dt = DDT_BF16 if logits.dtype == torch.bfloat16 else DDT_F32
+    rc = load().ddt_drafter_topk(rows, V, K, dt, _ptr(logits), _ptr(o["topk_logp"]),
+                                 _ptr(o["topk_ids"]), _stream(stream))
+    _check("ddt_drafter_topk", rc)
+    return o
 
 
 def ddt_cache_compact(kv_cache, block_table, prefix_len, accept_idx, accept_len, page_size: int,

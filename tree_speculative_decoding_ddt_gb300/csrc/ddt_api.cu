@@ -94,6 +94,16 @@ int run_attn(const ddt_attn_dims* d, const void* q_lat, const void* q_pe, const 
 }  // namespace
 
 namespace ddt {
+// SMs of the current device (cached per device).
+int device_sm_count() {
+  static int cached[64] = {};
+  int dev = 0, n = 148;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return n;
+  if (cached[dev] == 0 && cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+    cached[dev] = n;
+  return cached[dev] ? cached[dev] : n;
+}
+
 // Host checks of a verify-attention call (dims, then pointers and alignment),
 // shared with entry points defined in other files.
 int check_verify_attn_args(const ddt_attn_dims* d, const void* q_lat, const void* q_pe,
@@ -209,6 +219,15 @@ int ddt_target_argmax(int64_t rows, int64_t V, int dtype, const void* logits, in
   if (dtype != DDT_BF16 && dtype != DDT_F32) return DDT_EINVAL;
   if (rows > (int64_t(1) << 28) - 1 || V > 0x7fffffffLL) return DDT_EUNSUPPORTED;
   return launched(ddt::launch_target_argmax(rows, V, dtype, logits, argmax, stream));
+}
+
+int ddt_drafter_topk(int64_t rows, int64_t V, int32_t K, int dtype, const void* logits,
+                     float* topk_logp, int32_t* topk_ids, cudaStream_t stream) {
+  if (!logits || !topk_logp || !topk_ids || rows < 1 || V < 1 || K < 1) return DDT_EINVAL;
+  if (dtype != DDT_BF16 && dtype != DDT_F32) return DDT_EINVAL;
+  if (K > 16 || K > V || rows > (int64_t(1) << 28) - 1 || V > 0x7fffffffLL)
+    return DDT_EUNSUPPORTED;
+  return launched(ddt::launch_drafter_topk(rows, V, K, dtype, logits, topk_logp, topk_ids, stream));
 }
 
 size_t ddt_step_workspace_size(const ddt_step_args* args) {

@@ -100,6 +100,10 @@ int verify_attn_bf16_splits(const ddt_attn_dims& d);
 cudaError_t launch_target_argmax(long long rows, long long V, int dtype, const void* logits,
                                  int32_t* argmax, cudaStream_t stream);
 
+// Drafter-side log-softmax top-K over the vocabulary, one row per (sequence, depth).
+cudaError_t launch_drafter_topk(long long rows, long long V, int K, int dtype, const void* logits,
+                                float* topk_logp, int32_t* topk_ids, cudaStream_t stream);
+
 // Host checks of a verify-attention call (defined in ddt_api.cu).
 int check_verify_attn_args(const ddt_attn_dims* d, const void* q_lat, const void* q_pe,
                            const void* kv, const int32_t* block_table, const int32_t* prefix_len,
@@ -118,6 +122,34 @@ cudaError_t ensure_smem_limit(Kernel k, int bytes, int (&done)[64]) {
   e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess) done[dev] = bytes;
   return e;
+}
+
+// CTAs per row for the row-streaming kernels (argmax, top-K): the smallest
+// power of two up to `max_csize` that gives at least two CTAs per SM.
+int device_sm_count();
+inline unsigned row_cluster_size(long long rows, int max_csize) {
+  const long long want = 2LL * device_sm_count();
+  unsigned c = 1;
+  while ((long long)c * rows < want && (int)(2 * c) <= max_csize) c *= 2;
+  return c;
+}
+// Launch `kernel` over `grid` CTAs in clusters of `csize` (1: no cluster).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_rows(void (*kernel)(KArgs...), unsigned grid, unsigned csize, unsigned threads,
+                        cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = csize;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
 // ---- small device helpers ----------------------------------------------------

@@ -6,9 +6,9 @@
 // the step just upstream of accept: rows = tree slots of all sequences,
 // columns = the vocabulary.
 //
-// HBM-bound: every logit is read once. One 8-CTA cluster per row; each CTA
-// streams one eighth of the row with 16-byte loads (eight in flight per
-// thread). A thread scans its vectors in column order with about two
+// HBM-bound: every logit is read once. Each row is read by a cluster of 1 to
+// 8 CTAs (as many as keep about two CTAs per SM busy); each CTA streams its
+// share of the row with 16-byte loads (eight in flight per thread). A thread scans its vectors in column order with about two
 // instructions per logit (widen, NaN-propagating max per vector) and looks
 // for a column only when a vector beats its running best. The thread results
 // meet as 64-bit keys -- order-preserving value bits above the complemented
@@ -19,6 +19,7 @@
 #include <stdint.h>
 
 #include "ddt_internal.cuh"
+#include "order_keys.cuh"
 #include "sm100_ptx.cuh"
 
 namespace ddt {
@@ -27,28 +28,12 @@ namespace {
 using namespace sm100;
 
 constexpr int kThreads = 256;
-constexpr int kCluster = 8;
+constexpr int kMaxCluster = 8;
 constexpr int kInFlight = 8;  // 16-byte loads issued before any is used
 
-// Order-preserving 32-bit image of a logit: a larger value maps to a larger
-// image, -0.0 and +0.0 map to the same image, and every NaN maps above +inf.
-__device__ __forceinline__ uint32_t order_of(uint16_t h) {  // bf16 bits
-  if ((h & 0x7F80u) == 0x7F80u && (h & 0x007Fu)) return 0xFFFFFFFFu;
-  if (h == 0x8000u) h = 0;
-  return (h & 0x8000u) ? (uint32_t)(~h & 0xFFFFu) : (uint32_t)(h | 0x8000u);
-}
-__device__ __forceinline__ uint32_t order_of(uint32_t u) {  // f32 bits
-  if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return 0xFFFFFFFFu;
-  if (u == 0x80000000u) u = 0;
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-// key of the element at column `col`; the largest key wins
-__device__ __forceinline__ unsigned long long key_of(uint32_t ord, uint32_t col) {
-  return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - col);
-}
-__device__ __forceinline__ unsigned long long max_key(unsigned long long a, unsigned long long b) {
-  return a > b ? a : b;
-}
+using keys::key_of;
+using keys::max_key;
+using keys::order_of;
 
 __device__ __forceinline__ float max_nan(float a, float b) {  // NaN if either is NaN
   float r;
@@ -117,18 +102,19 @@ __device__ __forceinline__ unsigned long long ld_cluster_u64(uint32_t addr) {
 // vec: every row starts on a 16-byte boundary and V is a multiple of the
 // elements per 16 bytes, so the whole row is read with vector loads
 template <typename T>
-__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads)
     k_target_argmax(const T* __restrict__ logits, long long V, int vec, int32_t* __restrict__ out) {
   using E = Elems<T>;
   __shared__ unsigned long long s_warp[kThreads / 32];
   __shared__ unsigned long long s_cta;
-  const long long row = blockIdx.x / kCluster;
+  const uint32_t ncta = keys::cluster_size();  // the row's CTAs
+  const long long row = blockIdx.x / ncta;
   const uint32_t crank = cluster_rank();
   const int tid = threadIdx.x;
   const T* x = logits + row * V;
 
   // this CTA's columns [c0, c1): an eighth of the row, in whole vectors
-  const long long per = (((V + kCluster - 1) / kCluster) + E::kPerVec - 1) / E::kPerVec * E::kPerVec;
+  const long long per = (((V + ncta - 1) / ncta) + E::kPerVec - 1) / E::kPerVec * E::kPerVec;
   const long long c0 = min(V, (long long)crank * per);
   const long long c1 = min(V, c0 + per);
   Best bt;
@@ -188,9 +174,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
   if (crank == 0 && tid == 0) {
     unsigned long long b = s_cta;
     const uint32_t local = smem_u32(&s_cta);
-#pragma unroll
-    for (uint32_t r = 1; r < kCluster; ++r) b = max_key(b, ld_cluster_u64(map_peer(local, r)));
-    out[row] = (int32_t)(0xFFFFFFFFu - (uint32_t)(b & 0xFFFFFFFFull));
+    for (uint32_t r = 1; r < ncta; ++r) b = max_key(b, ld_cluster_u64(map_peer(local, r)));
+    out[row] = (int32_t)keys::col_of(b);
   }
   cluster_sync();  // the peers' shared memory stays valid until rank 0 has read it
 }
@@ -199,19 +184,16 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
 
 cudaError_t launch_target_argmax(long long rows, long long V, int dtype, const void* logits,
                                  int32_t* argmax, cudaStream_t stream) {
-  if (rows < 1 || V < 1 || rows * kCluster > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const unsigned csize = row_cluster_size(rows, kMaxCluster);
+  if (rows < 1 || V < 1 || rows * csize > 0x7fffffffLL) return cudaErrorInvalidValue;
   const bool aligned = (reinterpret_cast<uintptr_t>(logits) & 15u) == 0;
-  const unsigned grid = (unsigned)(rows * kCluster);
-  if (dtype == DDT_BF16) {
-    const int vec = aligned && V % 8 == 0;
-    k_target_argmax<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(logits), V, vec, argmax);
-  } else {
-    const int vec = aligned && V % 4 == 0;
-    k_target_argmax<float><<<grid, kThreads, 0, stream>>>(static_cast<const float*>(logits), V,
-                                                          vec, argmax);
-  }
-  return cudaGetLastError();
+  const unsigned grid = (unsigned)(rows * csize);
+  if (dtype == DDT_BF16)
+    return launch_rows(k_target_argmax<__nv_bfloat16>, grid, csize, kThreads, stream,
+                       static_cast<const __nv_bfloat16*>(logits), V, (int)(aligned && V % 8 == 0),
+                       argmax);
+  return launch_rows(k_target_argmax<float>, grid, csize, kThreads, stream,
+                     static_cast<const float*>(logits), V, (int)(aligned && V % 4 == 0), argmax);
 }
 
 }  // namespace ddt
