@@ -125,10 +125,11 @@ cudaError_t ensure_smem_limit(Kernel k, int bytes, int (&done)[64]) {
 }
 
 // CTAs per row for the row-streaming kernels (argmax, top-K): the smallest
-// power of two up to `max_csize` that gives at least two CTAs per SM.
+// power of two up to `max_csize` that puts at least one CTA on every SM.
+// Splitting further only adds per-CTA merges; fewer leaves SMs idle.
 int device_sm_count();
 inline unsigned row_cluster_size(long long rows, int max_csize) {
-  const long long want = 2LL * device_sm_count();
+  const long long want = device_sm_count();
   unsigned c = 1;
   while ((long long)c * rows < want && (int)(2 * c) <= max_csize) c *= 2;
   return c;
@@ -150,6 +151,15 @@ cudaError_t launch_rows(void (*kernel)(KArgs...), unsigned grid, unsigned csize,
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+// Launch a row-streaming kernel over `rows` rows, each row on a cluster of
+// row_cluster_size() CTAs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_row_kernel(void (*kernel)(KArgs...), long long rows, int max_csize,
+                              unsigned threads, cudaStream_t stream, Args... args) {
+  const unsigned csize = row_cluster_size(rows, max_csize);
+  if (rows < 1 || rows * csize > 0x7fffffffLL) return cudaErrorInvalidValue;
+  return launch_rows(kernel, (unsigned)(rows * csize), csize, threads, stream, args...);
 }
 
 // ---- small device helpers ----------------------------------------------------

@@ -8,15 +8,18 @@
 // vocabulary; per row the K largest logits (value descending, token id
 // ascending on ties) and logit - log(sum(exp(logits))).
 //
-// HBM-bound: every logit is read once. Each row is read by a cluster of 1 to
-// 8 CTAs (as many as keep about two CTAs per SM busy), each CTA streaming its
-// share of the row with 16-byte loads. A thread keeps an
-// online log-sum-exp (running max, rescaled sum, one exp2 per logit) and a
-// descending list of K ranking keys (order_keys.cuh; K rounded up to a power
-// of two), touched only when a vector's maximum beats the list's last key. Lists merge by K rounds
-// of "the largest head wins and its list advances": within a warp, across
-// the CTA's warps, then across the cluster's CTAs through distributed shared
-// memory, where the rank-0 CTA also combines the eight (max, sum) pairs.
+// HBM-bound: every logit is read once. Each row is read by a cluster of 1 to 8
+// CTAs (as few as still put a CTA on every SM), each CTA streaming its share
+// of the row with 16-byte loads. A thread keeps an online log-sum-exp (running
+// max, rescaled sum, one exp2 per logit) and a descending list of K ranking
+// keys (order_keys.cuh; K rounded up to a power of two), touched only when a
+// vector's maximum reaches both the list's last key and a lower bound on the
+// row's K-th value: first the K-th largest of the lanes' first maxima, then
+// the warp's K-th best, shared across the CTA through one shared-memory
+// maximum. Lists merge by K rounds of "the largest head wins and its list
+// advances": within a warp, across the CTA's warps, then across the cluster's
+// CTAs through distributed shared memory, where the rank-0 CTA also combines
+// the (max, sum) pairs.
 #include <cuda_bf16.h>
 #include <math.h>
 #include <stdint.h>
@@ -178,18 +181,44 @@ __device__ void warp_merge(TopK<KT>& t, int K, unsigned long long* out) {
     if (w != 0ull && t.k[0] == w) t.pop();
   }
 }
-// The K-th best key over the lists of all lanes of the warp (0 if the warp
-// has seen fewer than K logits). No logit ranked below it can be in the
-// row's top K, so it is a safe filter for every lane.
-template <typename E, int KT>
-__device__ unsigned long long warp_kth(const TopList<KT>& tl, int K) {
-  TopK<KT> t;
+// The K-th largest value over the lists of all lanes of the warp (-inf if
+// the warp has seen fewer than K logits). No logit below it can be in the
+// row's top K, so it is a safe filter for every lane. Values alone suffice
+// for a bound: K rounds of "the warp maximum of the heads, the lowest lane
+// holding it advances".
+template <int KT>
+__device__ float warp_kth(const TopList<KT>& tl, int K) {
+  float h[KT];
 #pragma unroll
-  for (int j = 0; j < KT; ++j) t.k[j] = tl.c[j] == kNone ? 0ull : key_of(E::ord(tl.v[j]), tl.c[j]);
-  unsigned long long w = 0ull;
+  for (int j = 0; j < KT; ++j) h[j] = tl.v[j];
+  const int lane = threadIdx.x & 31;
+  float w = -INFINITY;
   for (int r = 0; r < K; ++r) {
-    w = warp_max(t.k[0]);
-    if (w != 0ull && t.k[0] == w) t.pop();
+    w = h[0];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) w = fmaxf(w, __shfl_xor_sync(0xffffffffu, w, off));
+    const unsigned holders = __ballot_sync(0xffffffffu, h[0] == w);
+    if (lane == __ffs(holders) - 1) {
+#pragma unroll
+      for (int j = 0; j < KT - 1; ++j) h[j] = h[j + 1];
+      h[KT - 1] = -INFINITY;
+    }
+  }
+  return w;
+}
+
+// The K-th largest of the lanes' values x (-inf if fewer than K lanes hold a
+// number): K rounds of "take the warp maximum, the lowest lane holding it
+// drops out".
+__device__ float warp_kth_value(float x, int K) {
+  const int lane = threadIdx.x & 31;
+  float w = -INFINITY;
+  for (int r = 0; r < K; ++r) {
+    w = x;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) w = fmaxf(w, __shfl_xor_sync(0xffffffffu, w, off));
+    const unsigned holders = __ballot_sync(0xffffffffu, x == w);
+    if (lane == __ffs(holders) - 1) x = -INFINITY;
   }
   return w;
 }
@@ -221,6 +250,9 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ float s_wm[kWarps], s_ws[kWarps];
   __shared__ unsigned long long s_cta[kMaxK];
   __shared__ float s_cm, s_cs;
+  // the best lower bound on the row's K-th value that a warp of this CTA has
+  // found, as an order image of its f32 bits (order_keys.cuh)
+  __shared__ uint32_t s_thr;
   const uint32_t ncta = keys::cluster_size();  // the row's CTAs
   const long long row = blockIdx.x / ncta;
   const uint32_t crank = cluster_rank();
@@ -233,7 +265,9 @@ __global__ void __launch_bounds__(kThreads)
   TopList<KT> tl;
   tl.clear();
   Lse ls;
-  float wthr = -INFINITY;  // the warp's K-th best so far (a lower bound on the row's)
+  float wthr = -INFINITY;  // a lower bound on the row's K-th value (the filter)
+  if (tid == 0) s_thr = order_of(__float_as_uint(-INFINITY));
+  __syncthreads();
   if (vec) {
     const long long nv = (c1 - c0) / E::kPerVec;
     const uint4* xv = reinterpret_cast<const uint4*>(x + c0);
@@ -243,6 +277,21 @@ __global__ void __launch_bounds__(kThreads)
       for (int k = 0; k < kInFlight; ++k) {
         const long long i = base + tid + (long long)k * kThreads;
         if (i < nv) v[k] = ld_stream(xv + i);
+      }
+      if (base == 0) {
+        // before any list exists: the maxima of the lanes' first vectors
+        // are distinct logits, so the K-th largest of them bounds the row's
+        // K-th value from below and spares the lanes most first inserts
+        float lm = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kInFlight; ++k) {
+          if (base + tid + (long long)k * kThreads >= nv) continue;
+          float f[E::kPerVec];
+          E::unpack(v[k], f);
+#pragma unroll
+          for (int j = 0; j < E::kPerVec; ++j) lm = fmaxf(lm, f[j]);
+        }
+        wthr = warp_kth_value(lm, K);
       }
 #pragma unroll
       for (int k = 0; k < kInFlight; ++k) {
@@ -265,8 +314,8 @@ __global__ void __launch_bounds__(kThreads)
           ls.s += acc;
         }
         // the list changes only if the vector reaches both the list's last
-        // value and the warp's K-th best (ties still go through: the column
-        // decides them)
+        // value and the lower bound on the row's K-th value (ties still go
+        // through: the column decides them)
         if (vm >= fmaxf(tl.last(), wthr)) {
           const uint32_t col0 = (uint32_t)(c0 + i * E::kPerVec);
           // visit only the elements that reach the filter (usually one),
@@ -286,8 +335,11 @@ __global__ void __launch_bounds__(kThreads)
       // a lane alone sees few logits, so its own K-th best stays low and some
       // lane of the warp would take the insert path at nearly every vector:
       // tighten every lane's filter to the warp's K-th best
-      const unsigned long long wk = warp_kth<E>(tl, K);
-      if (wk != 0ull) wthr = E::value((uint32_t)(wk >> 32));
+      wthr = fmaxf(wthr, warp_kth(tl, K));
+      // and share the bound with the CTA's other warps
+      if (lane == 0) atomicMax(&s_thr, order_of(__float_as_uint(wthr)));
+      __syncwarp();
+      wthr = fmaxf(wthr, keys::value_of_f32(*static_cast<volatile uint32_t*>(&s_thr)));
     }
   } else {
     for (long long c = c0 + tid; c < c1; c += kThreads) {
@@ -375,20 +427,17 @@ __global__ void __launch_bounds__(kThreads)
 
 cudaError_t launch_drafter_topk(long long rows, long long V, int K, int dtype, const void* logits,
                                 float* topk_logp, int32_t* topk_ids, cudaStream_t stream) {
-  const unsigned csize = row_cluster_size(rows, kMaxCluster);
-  if (rows < 1 || V < 1 || K < 1 || K > kMaxK || K > V || rows * csize > 0x7fffffffLL)
-    return cudaErrorInvalidValue;
+  if (rows < 1 || V < 1 || K < 1 || K > kMaxK || K > V) return cudaErrorInvalidValue;
   const bool aligned = (reinterpret_cast<uintptr_t>(logits) & 15u) == 0;
-  const unsigned grid = (unsigned)(rows * csize);
   const int vb = aligned && V % 8 == 0, vf = aligned && V % 4 == 0;
   const __nv_bfloat16* lb = static_cast<const __nv_bfloat16*>(logits);
   const float* lf = static_cast<const float*>(logits);
 #define DDT_TOPK_LAUNCH(KT)                                                                      \
   return dtype == DDT_BF16                                                                       \
-             ? launch_rows(k_drafter_topk<__nv_bfloat16, KT>, grid, csize, kThreads, stream, lb, \
-                           V, K, vb, topk_logp, topk_ids)                                        \
-             : launch_rows(k_drafter_topk<float, KT>, grid, csize, kThreads, stream, lf, V, K,   \
-                           vf, topk_logp, topk_ids);
+             ? launch_row_kernel(k_drafter_topk<__nv_bfloat16, KT>, rows, kMaxCluster,      \
+                                 kThreads, stream, lb, V, K, vb, topk_logp, topk_ids)            \
+             : launch_row_kernel(k_drafter_topk<float, KT>, rows, kMaxCluster, kThreads,      \
+                                 stream, lf, V, K, vf, topk_logp, topk_ids);
   if (K <= 1) DDT_TOPK_LAUNCH(1)
   if (K <= 2) DDT_TOPK_LAUNCH(2)
   if (K <= 4) DDT_TOPK_LAUNCH(4)

@@ -6,15 +6,15 @@
 // the step just upstream of accept: rows = tree slots of all sequences,
 // columns = the vocabulary.
 //
-// HBM-bound: every logit is read once. Each row is read by a cluster of 1 to
-// 8 CTAs (as many as keep about two CTAs per SM busy); each CTA streams its
-// share of the row with 16-byte loads (eight in flight per thread). A thread scans its vectors in column order with about two
-// instructions per logit (widen, NaN-propagating max per vector) and looks
-// for a column only when a vector beats its running best. The thread results
-// meet as 64-bit keys -- order-preserving value bits above the complemented
-// column, so the largest key is the largest value at the lowest column -- in
-// warp, CTA and finally the rank-0 CTA of the cluster through distributed
-// shared memory. One launch, no scratch memory.
+// HBM-bound: every logit is read once. Each row is read by a cluster of 1 to 8
+// CTAs (as few as still put a CTA on every SM); each CTA streams its share of
+// the row with 16-byte loads (eight in flight per thread). A thread scans its
+// vectors in column order with about two instructions per logit (widen, NaN-
+// propagating max per vector) and looks for a column only when a vector beats
+// its running best. The thread results meet as 64-bit keys -- order-preserving
+// value bits above the complemented column, so the largest key is the largest
+// value at the lowest column -- in warp, CTA and finally the rank-0 CTA of the
+// cluster through distributed shared memory. One launch, no scratch memory.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -184,16 +184,15 @@ __global__ void __launch_bounds__(kThreads)
 
 cudaError_t launch_target_argmax(long long rows, long long V, int dtype, const void* logits,
                                  int32_t* argmax, cudaStream_t stream) {
-  const unsigned csize = row_cluster_size(rows, kMaxCluster);
-  if (rows < 1 || V < 1 || rows * csize > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (rows < 1 || V < 1) return cudaErrorInvalidValue;
   const bool aligned = (reinterpret_cast<uintptr_t>(logits) & 15u) == 0;
-  const unsigned grid = (unsigned)(rows * csize);
   if (dtype == DDT_BF16)
-    return launch_rows(k_target_argmax<__nv_bfloat16>, grid, csize, kThreads, stream,
-                       static_cast<const __nv_bfloat16*>(logits), V, (int)(aligned && V % 8 == 0),
-                       argmax);
-  return launch_rows(k_target_argmax<float>, grid, csize, kThreads, stream,
-                     static_cast<const float*>(logits), V, (int)(aligned && V % 4 == 0), argmax);
+    return launch_row_kernel(k_target_argmax<__nv_bfloat16>, rows, kMaxCluster, kThreads, stream,
+                             static_cast<const __nv_bfloat16*>(logits), V,
+                             (int)(aligned && V % 8 == 0), argmax);
+  return launch_row_kernel(k_target_argmax<float>, rows, kMaxCluster, kThreads, stream,
+                           static_cast<const float*>(logits), V, (int)(aligned && V % 4 == 0),
+                           argmax);
 }
 
 }  // namespace ddt
