@@ -11,6 +11,9 @@ step, written for checking the CUDA path and never called by it:
                            input of tree_accept, one step upstream)
 * :func:`drafter_topk`     the drafter's per-depth top-K log-probs (the input
                            of tree_build, one step upstream)
+* :func:`rope_append`      NeoX rotary embedding of the tree's rope parts at
+                           positions L+depth and the append of the tree
+                           latents to the cache (just before the attention)
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this module. It shares no code with the CUDA path:
@@ -53,7 +56,14 @@ Readings of points the sources leave open (each one is listed in the design doc):
 * accept follows the lowest-index child whose token equals the target argmax
   at its parent, at most ``D`` hops, and stops with ``ST_CYCLE`` if it would
   revisit a node;
-* compaction reads every source row before writing any destination row.
+* compaction reads every source row before writing any destination row;
+* rotary embedding: the NeoX pairing (i, i + R/2) with frequencies
+  ``theta ** (-2i/R)`` and base ``theta`` a parameter (YaRN scaling is out of
+  scope); a tree slot's position is ``L + depth`` and a padding slot
+  (depth -1) takes position ``L``; the tree latents of slot t go to cache
+  slot ``L + t`` with their rope part rotated and their latent part copied;
+  a sequence whose slots ``[L, L+Q)`` leave its pages or the cache is left
+  untouched with the capacity / range status bit.
 """
 from __future__ import annotations
 
@@ -422,6 +432,85 @@ def drafter_topk(logits, K: int):
         ids[r] = order.astype(np.int32)
         logp[r] = (row[order] - lse).astype(np.float32)
     return logp.reshape(lead + (K,)), ids.reshape(lead + (K,))
+
+
+# ================================ tree positions: rotary embedding + append
+
+def rope_inv_freq(R: int, theta: float) -> np.ndarray:
+    """Rotary frequencies of a rope part of width R (even): ``theta ** (-2i/R)``
+    for i in [0, R/2), float64. "The Consolidation Point: Validating Generality
+    and Wrapping the MVP", "The Journey to This Point" (NeoX-style rotary
+    position embeddings in the engine's layers)."""
+    i = np.arange(R // 2, dtype=np.float64)
+    return np.power(float(theta), -2.0 * i / R)
+
+
+def rope_neox(x, pos, theta: float) -> np.ndarray:
+    """NeoX rotation of the last axis of ``x`` at position ``pos`` (a number,
+    or an array broadcasting against ``x``'s leading axes), float64.
+
+    The last axis holds R/2 pairs (x_i, x_{i+R/2}); pair i turns by the angle
+    ``pos * theta**(-2i/R)``:
+    ``y_i = x_i cos - x_{i+R/2} sin`` and ``y_{i+R/2} = x_{i+R/2} cos + x_i sin``.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    R = x.shape[-1]
+    h = R // 2
+    ang = np.asarray(pos, dtype=np.float64)[..., None] * rope_inv_freq(R, theta)
+    c, s = np.cos(ang), np.sin(ang)
+    lo, hi = x[..., :h], x[..., h:]
+    return np.concatenate([lo * c - hi * s, hi * c + lo * s], axis=-1)
+
+
+def rope_append(q_pe, kv_new, kv, block_table, prefix_len, depths, page_size: int,
+                theta: float):
+    """The tree's rotary embedding and cache append, one verify step.
+
+    "The Checkpoint: Committing a Working Native DDTree Engine", "The
+    Message": the tree [verified_id, drafts] is processed at positions
+    L+depth with prefix = cache length (KV-cache scheme), and the engine's
+    model does "cache append" of the new latents before attention (rope is one
+    of its ops); "The Consolidation Point", "The Journey to This Point":
+    the rotary embedding is the NeoX kind.
+
+    Shapes: q_pe [B,Q,H,R], kv_new [B,Q,C+R] (latent part then unrotated rope
+    part), kv [rows, C+R] (the paged cache, not modified), block_table
+    [B, max_pages], prefix_len [B], depths [B,Q] (-1 = padding slot).
+    For sequence b (L = prefix_len[b]) and slot t: position
+    p = L + max(depths[b,t], 0); q_out[b,t] = rope(q_pe[b,t], p) for every
+    head; cache slot L + t receives kv_new[b,t] with its last R values
+    replaced by rope(them, p). A sequence with L < 0 or L + Q beyond its
+    pages gets ST_CAPACITY, one whose pages leave the cache gets ST_RANGE;
+    either way nothing of it is written (its q_out rows are NaN here).
+
+    Returns (q_out float64 [B,Q,H,R], kv_out float64 copy of kv with the
+    appended rows, status int32 [B]).
+    """
+    q_pe = np.asarray(q_pe, dtype=np.float64)
+    kv_new = np.asarray(kv_new, dtype=np.float64)
+    B, Q, H, R = q_pe.shape
+    CR = kv_new.shape[-1]
+    C = CR - R
+    kv_out = np.array(kv, dtype=np.float64, copy=True)
+    rows = kv_out.shape[0]
+    max_pages = block_table.shape[1]
+    q_out = np.full(q_pe.shape, np.nan)
+    status = np.zeros(B, np.int32)
+    for b in range(B):
+        L = int(prefix_len[b])
+        if L < 0 or L + Q > max_pages * page_size:
+            status[b] |= ST_CAPACITY
+            continue
+        phys = slot_rows(block_table[b], page_size, np.arange(L, L + Q))
+        if (phys < 0).any() or (phys >= rows).any():
+            status[b] |= ST_RANGE
+            continue
+        for t in range(Q):
+            p = L + max(int(depths[b][t]), 0)
+            q_out[b, t] = rope_neox(q_pe[b, t], p, theta)
+            kv_out[phys[t], :C] = kv_new[b, t, :C]
+            kv_out[phys[t], C:] = rope_neox(kv_new[b, t, C:], p, theta)
+    return q_out, kv_out, status
 
 
 # =================================================== multi-step decode (loop)
