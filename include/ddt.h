@@ -328,6 +328,43 @@ int ddt_target_argmax(int64_t rows, int64_t V, int dtype, const void* logits, in
 int ddt_drafter_topk(int64_t rows, int64_t V, int32_t K, int dtype, const void* logits,
                      float* topk_logp, int32_t* topk_ids, cudaStream_t stream);
 
+/* Rotary embedding of the tree at positions L+depth and append of the tree
+ * latents to the paged cache (the step between the target's projections and
+ * ddt_verify_attn).
+ * "The Checkpoint: Committing a Working Native DDTree Engine", section "The
+ * Message" (KV-cache scheme: [verified_id, drafts] processed at positions
+ * L+depth, prefix = cache length; the model's cache append before
+ * attention); "The Consolidation Point: Validating Generality and Wrapping
+ * the MVP", section "The Journey to This Point" (NeoX-style rotary
+ * embedding).
+ *
+ * dims: B, Q, H, C, R, page_size, max_pages, dtype and kv_rows as in
+ * ddt_attn_dims (scale and max_len are not used); R even, 2 <= R <= 256,
+ * C >= 0, any page_size >= 1. theta: the rotary base (> 0, finite).
+ * For sequence b (L = prefix_len[b]) and tree slot t the position is
+ * p = L + max(depths[b][t], 0) (padding slots, depth -1, take L); pair i of
+ * a rope part, (x_i, x_{i+R/2}), turns by p * theta^(-2i/R):
+ *   y_i = x_i cos - x_{i+R/2} sin,  y_{i+R/2} = x_{i+R/2} cos + x_i sin.
+ * q_pe_in [B][Q][H][R] -> q_pe_out [B][Q][H][R] (the same pointer rotates in
+ * place; otherwise the buffers must not overlap). kv_new [B][Q][C+R] (latent
+ * part, then the unrotated rope part) -> cache slot L + t of kv_cache
+ * [kv_rows][C+R] (paged through block_table i32[B][max_pages]), latent part
+ * copied bit for bit and rope part rotated; kv_new must not overlap the
+ * cache. The angles are formed in double and reduced modulo 2*pi before a
+ * float sine and cosine, the pairs turn in fp32 and are rounded once to the
+ * element type: within 1e-6 * (|x_i| + |x_{i+R/2}|) of the exact rotation
+ * before that rounding. A sequence with L < 0 or L + Q > max_pages *
+ * page_size gets DDT_ST_CAPACITY, one with a slot of [L, L+Q) on a page
+ * outside the kv_rows rows DDT_ST_RANGE (status i32[B], OR-ed); nothing of
+ * it is written. All pointers are caller-owned device memory. Limits:
+ * 1 <= Q <= DDT_MAX_Q, B * Q <= 2^31 - 1. Returns DDT_EINVAL for a null
+ * pointer, a bad size, an odd R or a bad theta, DDT_EUNSUPPORTED past the
+ * limits. Enqueues one kernel; allocates nothing. */
+int ddt_rope_append(const ddt_attn_dims* dims, double theta, const int32_t* depths,
+                    const int32_t* prefix_len, const int32_t* block_table, const void* q_pe_in,
+                    void* q_pe_out, const void* kv_new, void* kv_cache, int32_t* status,
+                    cudaStream_t stream);
+
 /* Static text for a DDT_E* return code. */
 const char* ddt_strerror(int code);
 

@@ -73,6 +73,7 @@ SIGNATURES = {
                                          _P]),
     "ddt_drafter_topk": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
                                         ctypes.c_int, _P, _P, _P, _P]),
+    "ddt_rope_append": (ctypes.c_int, [ctypes.POINTER(AttnDims), ctypes.c_double] + [_P] * 9),
     "ddt_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "ddt_abi_version": (ctypes.c_int, []),
 }
@@ -317,6 +318,42 @@ def ddt_drafter_topk(logits: torch.Tensor, K: int, out: Optional[dict] = None,
                                  _ptr(o["topk_ids"]), _stream(stream))
     _check("ddt_drafter_topk", rc)
     return o
+
+
+def ddt_rope_append(q_pe, kv_new, kv_cache, block_table, prefix_len, depths, page_size: int,
+                    theta: float = 10000.0, q_out=None, status=None, stream=None):
+    """Rotary embedding of the tree at positions ``prefix_len + depth`` and
+    append of the tree latents to the paged cache. ``q_pe`` [B,Q,H,R] (turned
+    into ``q_out``; ``q_out=q_pe`` rotates in place), ``kv_new`` [B,Q,C+R]
+    (latent part, then the unrotated rope part) written to cache slots
+    ``[L, L+Q)`` of ``kv_cache`` [rows, C+R]; ``depths`` int32 [B,Q] from the
+    tree build. Returns (q_out, status)."""
+    B, Q, H, R = q_pe.shape
+    dt = q_pe.dtype
+    if dt not in (torch.float32, torch.bfloat16):
+        raise TypeError("q_pe must be float32 or bfloat16")
+    _need(q_pe, "q_pe", dt)
+    CR = int(kv_new.shape[-1])
+    _need(kv_new, "kv_new", dt, (B, Q, CR))
+    _need(kv_cache, "kv_cache", dt)
+    if kv_cache.dim() != 2 or kv_cache.shape[1] != CR:
+        raise ValueError("kv_cache must be [rows, C+R]")
+    _need(block_table, "block_table", torch.int32)
+    _need(prefix_len, "prefix_len", torch.int32, (B,))
+    _need(depths, "depths", torch.int32, (B, Q))
+    dev = q_pe.device
+    if q_out is None:
+        q_out = torch.empty_like(q_pe)
+    _need(q_out, "q_out", dt, (B, Q, H, R))
+    if status is None:
+        status = torch.zeros((B,), dtype=torch.int32, device=dev)
+    dims = attn_dims(B, Q, H, CR - R, R, page_size, block_table.shape[1], kv_cache.shape[0],
+                     DDT_F32 if dt == torch.float32 else DDT_BF16, 1.0, 0)
+    rc = load().ddt_rope_append(ctypes.byref(dims), float(theta), _ptr(depths), _ptr(prefix_len),
+                                _ptr(block_table), _ptr(q_pe), _ptr(q_out), _ptr(kv_new),
+                                _ptr(kv_cache), _ptr(status), _stream(stream))
+    _check("ddt_rope_append", rc)
+    return q_out, status
 
 
 def ddt_cache_compact(kv_cache, block_table, prefix_len, accept_idx, accept_len, page_size: int,

@@ -230,6 +230,26 @@ int ddt_drafter_topk(int64_t rows, int64_t V, int32_t K, int dtype, const void* 
   return launched(ddt::launch_drafter_topk(rows, V, K, dtype, logits, topk_logp, topk_ids, stream));
 }
 
+int ddt_rope_append(const ddt_attn_dims* d, double theta, const int32_t* depths,
+                    const int32_t* prefix_len, const int32_t* block_table, const void* q_pe_in,
+                    void* q_pe_out, const void* kv_new, void* kv_cache, int32_t* status,
+                    cudaStream_t stream) {
+  if (d == nullptr || !depths || !prefix_len || !block_table || !q_pe_in || !q_pe_out || !kv_new ||
+      !kv_cache || !status)
+    return DDT_EINVAL;
+  if (d->B < 1 || d->Q < 1 || d->H < 1 || d->C < 0 || d->R < 2 || d->R % 2 != 0 ||
+      d->page_size < 1 || d->max_pages < 1 || d->kv_rows < 0 || !(theta > 0.0) ||
+      !isfinite(theta))
+    return DDT_EINVAL;
+  if (d->dtype != DDT_BF16 && d->dtype != DDT_F32) return DDT_EINVAL;
+  if (d->Q > DDT_MAX_Q || d->R / 2 > ddt::kMaxRopeHalf || (int64_t)d->B * d->Q > 0x7fffffffLL)
+    return DDT_EUNSUPPORTED;
+  ddt::RopeFreqs f = {};
+  for (int i = 0; i < d->R / 2; ++i) f.f[i] = pow(theta, -2.0 * i / d->R);
+  return launched(ddt::launch_rope_append(*d, f, depths, prefix_len, block_table, q_pe_in,
+                                          q_pe_out, kv_new, kv_cache, status, stream));
+}
+
 size_t ddt_step_workspace_size(const ddt_step_args* args) {
   if (args == nullptr) return 0;
   return ddt_verify_attn_workspace_size(&args->attn);

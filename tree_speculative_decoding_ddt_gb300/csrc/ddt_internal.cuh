@@ -134,6 +134,17 @@ inline unsigned row_cluster_size(long long rows, int max_csize) {
   while ((long long)c * rows < want && (int)(2 * c) <= max_csize) c *= 2;
   return c;
 }
+// Rotary frequencies theta^(-2i/R), i < R/2, computed on the host in double
+// and passed by value to the rope kernel.
+constexpr int kMaxRopeHalf = 128;
+struct RopeFreqs {
+  double f[kMaxRopeHalf];
+};
+cudaError_t launch_rope_append(const ddt_attn_dims& d, const RopeFreqs& freqs,
+                               const int32_t* depths, const int32_t* prefix_len,
+                               const int32_t* block_table, const void* q_in, void* q_out,
+                               const void* kv_new, void* kv, int32_t* status, cudaStream_t stream);
+
 // Launch `kernel` over `grid` CTAs in clusters of `csize` (1: no cluster).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_rows(void (*kernel)(KArgs...), unsigned grid, unsigned csize, unsigned threads,
