@@ -280,11 +280,29 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ GPU arm
 
-def time_next_rows(w, dev, stream, flush, n: int) -> dict:
+def _event_median_s(fn, stream, flush, n: int) -> float:
+    """Median device time of ``fn`` over n launches, L2 flushed before each."""
+    import torch
+    fn()
+    ts = []
+    for _ in range(max(5, min(n, 50))):
+        flush.fill_(1)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn()
+        e.record(stream)
+        ts.append((s, e))
+    torch.cuda.synchronize()
+    return statistics.median([s.elapsed_time(e) for s, e in ts]) / 1e3
+
+
+def time_next_rows(w, dev, stream, flush, n: int, buf=None) -> dict:
     """Event-timed launches of the steps next to the verify step on this
     workload's shapes (L2 flushed before each launch), each against the HBM
     roofline of its algorithmic bytes: the target-side argmax over
-    B*Q x V logits and the drafter's top-K over B*D x V logits."""
+    B*Q x V logits, the drafter's top-K over B*D x V logits and (given the
+    step's buffers) the rotary embedding and cache append of the tree at its
+    positions L+depth."""
     import torch
     from tree_speculative_decoding_ddt_gb300 import _binding as DB
     hbm, _, src = measured_peaks()
@@ -332,6 +350,29 @@ def time_next_rows(w, dev, stream, flush, n: int) -> dict:
                            "algorithmic_bytes": byt, "peak_source": src,
                            "data": "seeded device normal logits"}
     del dl
+    if buf is not None:
+        # rotary embedding + append on the step's own cache, pages and tree
+        # depths (the tree the timed steps built); q turned into a separate
+        # buffer, new latents drawn on the device
+        ldt = buf.q_pe.dtype
+        kv_new = torch.randn((w.B, w.Q, w.C + w.R), generator=gen, device=dev).to(ldt)
+        q_out = torch.empty_like(buf.q_pe)
+        st = torch.zeros((w.B,), dtype=torch.int32, device=dev)
+        ps = buf.attn.page_size
+        sec = _event_median_s(lambda: DB.ddt_rope_append(
+            buf.q_pe, kv_new, buf.kv_cache, buf.block_table, buf.prefix_len, buf.depths, ps,
+            q_out=q_out, status=st), stream, flush, n)
+        es = buf.q_pe.element_size()
+        byt = w.B * w.Q * (2 * w.H * w.R + 2 * (w.C + w.R)) * es + w.B * w.Q * 4
+        out["rope_append"] = {"kernel": "k_rope_append", "slots": w.B * w.Q, "H": w.H, "R": w.R,
+                              "us": sec * 1e6, "bound": "hbm", "achieved": byt / sec / 1e9,
+                              "peak": hbm, "unit": "GB/s", "frac": byt / sec / 1e9 / hbm,
+                              "algorithmic_bytes": byt, "peak_source": src,
+                              "data": "the step's cache, pages and tree depths; seeded "
+                                      "device latents"}
+        if int(st.abs().sum()) != 0:
+            raise SystemExit(f"rope_append status reports errors: {st.cpu().numpy()}")
+        del kv_new, q_out
     return out
 
 
@@ -438,7 +479,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         attn_ms = [s.elapsed_time(e) for s, e in aevs]
         # the next rows of the path, on this workload's shapes, timed the same way
-        next_rows = time_next_rows(w, dev, stream, flush, n_attn)
+        next_rows = time_next_rows(w, dev, stream, flush, n_attn, buf)
     clocks = clk.summary()
 
     # end to end through the public API: host inputs in pinned memory are

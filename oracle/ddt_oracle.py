@@ -14,6 +14,8 @@ step, written for checking the CUDA path and never called by it:
 * :func:`rope_append`      NeoX rotary embedding of the tree's rope parts at
                            positions L+depth and the append of the tree
                            latents to the cache (just before the attention)
+* :func:`decode_loop_table` the multi-step DDTree decode loop with a table
+                           drafter (per-position logits) and a stream target
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this module. It shares no code with the CUDA path:
@@ -575,5 +577,70 @@ def decode_loop(golden: list, n_new: int, D: int, K: int, budget: int, V: int,
         acc = accept_one(tree["tokens"], tree["parents"], target, D)
         committed.extend(acc["out_tokens"][: acc["accept_len"] + 1])
         per_step.append(acc["accept_len"] + 1)
+        steps += 1
+    return committed[: n_new + 1], steps, per_step
+
+
+def ar_decode(golden, n_new: int, V: int) -> list:
+    """Autoregressive greedy decoding against the stream target: one target
+    step per token, each committing the target's greedy token after the
+    context so far (the stream's next token while the context follows the
+    stream, else V-1)."""
+    out = [int(golden[0])]
+    on_stream = True
+    while len(out) < n_new + 1:
+        nxt = len(out)
+        on_stream = on_stream and out[-1] == int(golden[nxt - 1])
+        out.append(int(golden[nxt]) if on_stream and nxt < len(golden) else V - 1)
+    return out
+
+
+def decode_loop_table(golden, table, n_new: int, D: int, K: int, budget: int, V: int,
+                      max_steps: int):
+    """The DDTree decode loop of one sequence, as the native engine's
+    generate_ddtree runs it ("The Checkpoint: Committing a Working Native DDTree
+    Engine", "The Message": tree_build -> verify -> tree_accept + cache
+    compaction per step, with a drafter interface; "DDTree greedy == AR ==
+    golden" and the oracle drafter's 8.00 accepted tokens per step).
+
+    Drafter: the row for depth d (1..D) is ``table[n - 1 + d]`` (row g holds
+    the logits for stream position g; n = tokens committed so far), turned
+    into candidates by :func:`drafter_topk`. Target: at a tree node whose
+    path from the root follows the stream, the greedy token is the stream's
+    next token, elsewhere V-1. Each step commits the accepted drafts and the
+    bonus token; the bonus is the next step's root. Stops once ``n_new``
+    tokens follow the first or after ``max_steps`` steps.
+
+    Returns (committed tokens [<= n_new+1], steps, tokens committed by each
+    step before the final truncation).
+    """
+    golden = [int(x) for x in golden]
+    G = len(golden)
+    committed = [golden[0]]
+    per_step = []
+    steps = 0
+    while len(committed) < n_new + 1 and steps < max_steps:
+        n = len(committed)
+        rows = np.stack([table[min(n - 1 + d, G - 1)] for d in range(1, D + 1)])
+        logp, ids = drafter_topk(rows, K)
+        tree = build_one(logp, ids, committed[-1], budget, V)
+        Q = budget + 1
+        target = np.full(Q, V - 1, np.int64)
+        for s in range(Q):
+            dep = tree["depths"][s]
+            if dep < 0:
+                continue
+            c, ok = s, True
+            while c > 0:
+                dc = tree["depths"][c]
+                if tree["tokens"][c] != golden[min(n - 1 + dc, G - 1)]:
+                    ok = False
+                c = tree["parents"][c]
+            if ok and n + dep < G:
+                target[s] = golden[n + dep]
+        acc = accept_one(tree["tokens"], tree["parents"], target, D)
+        k = acc["accept_len"] + 1
+        committed.extend(acc["out_tokens"][:k])
+        per_step.append(k)
         steps += 1
     return committed[: n_new + 1], steps, per_step

@@ -18,6 +18,10 @@ stream   what it draws
 2        synthetic target: match draws and fallback tokens
 3        batch-level draws (prefix lengths, page shuffle, match rates)
 4        root token
+5        target logits
+6        drafter logits
+7        decode loop: golden token streams
+8        decode loop: drafter table (noise and hit draws)
 =======  ==============================================
 
 The workloads follow the pages' setting: Kimi K2.6 MLA dimensions
@@ -42,6 +46,8 @@ STREAM_BATCH = 3
 STREAM_ROOT = 4
 STREAM_TARGET_LOGITS = 5
 STREAM_DRAFTER_LOGITS = 6
+STREAM_LOOP_GOLDEN = 7
+STREAM_LOOP_DRAFTER = 8
 
 #: rows of the latent cache generated per random-number call (keeps peak host
 #: memory bounded and lets any row block be regenerated on its own)
@@ -383,4 +389,41 @@ def target_argmax_for(batch: Batch, depths: np.ndarray) -> np.ndarray:
     for b in range(w.B):
         out[b] = synth_target_argmax(depths[b], batch.topk_ids[b], batch.target_u[b],
                                      batch.target_fallback[b], float(batch.match_p[b]))
+    return out
+
+
+# ------------------------------------------------------------------ decode loop
+
+def loop_golden(cid: int, B: int, G: int, V: int) -> np.ndarray:
+    """int32 [B, G]: the synthetic target's greedy token stream of every
+    sequence (its continuation of any context that follows the stream).
+    Tokens lie in [0, V-1): V-1 is left for the target's answer after a
+    context that left the stream."""
+    out = np.zeros((B, G), np.int32)
+    for b in range(B):
+        out[b] = rng(cid, b, STREAM_LOOP_GOLDEN).integers(0, max(V - 1, 1), G)
+    return out
+
+
+def loop_drafter_table(cid: int, golden: np.ndarray, V: int, hit, dtype: str,
+                       spike: float = 8.0) -> np.ndarray:
+    """float32 [B, G, V]: the synthetic drafter's logits for the token at
+    stream position g of sequence b (row g predicts golden[b, g]). Unit
+    normal noise; with probability ``hit`` (a number, or one per sequence)
+    the golden token is raised ``spike`` above the row's largest noise value,
+    so it is the drafter's first candidate. bf16-representable for bf16."""
+    B, G = golden.shape
+    hits = np.broadcast_to(np.asarray(hit, np.float64), (B,))
+    out = np.empty((B, G, V), np.float32)
+    for b in range(B):
+        g = rng(cid, b, STREAM_LOOP_DRAFTER)
+        rows = g.standard_normal((G, V), dtype=np.float32)
+        if dtype == "bf16":
+            rows = round_bf16(rows)
+        draw = g.random(G)
+        for j in range(G):
+            if draw[j] < hits[b]:
+                top = np.array([rows[j].max() + spike], np.float32)
+                rows[j, golden[b, j]] = (round_bf16(top) if dtype == "bf16" else top)[0]
+        out[b] = rows
     return out
