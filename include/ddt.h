@@ -365,6 +365,77 @@ int ddt_rope_append(const ddt_attn_dims* dims, double theta, const int32_t* dept
                     void* q_pe_out, const void* kv_new, void* kv_cache, int32_t* status,
                     cudaStream_t stream);
 
+/* ---- multi-step decode loop ------------------------------------------------
+ * DDTree greedy decoding of several tokens per sequence, all steps on the
+ * device: one CUDA graph whose conditional WHILE node repeats a verify step
+ * until every sequence has n_new tokens after its first, or max_steps steps
+ * have run.
+ * "The Checkpoint: Committing a Working Native DDTree Engine", section "The
+ * Message" (generate_ddtree wires tree_build -> verify_attn -> tree_accept +
+ * cache compaction with a drafter interface; DDTree greedy == AR greedy; the
+ * oracle drafter accepts 8.00 tokens per step, 3 verify steps for 24 tokens).
+ *
+ * A step: the drafter's logits for depths 1..D -> ddt_drafter_topk ->
+ * ddt_tree_build (root = last committed token) -> ddt_rope_append ->
+ * ddt_verify_attn -> the target's logits at every tree slot ->
+ * ddt_target_argmax -> accept + compaction -> commit (accepted drafts, then
+ * the bonus token, which is the next root; the cache length becomes the
+ * compacted length).
+ * The two model interfaces are synthetic stand-ins: the DRAFTER's logits
+ * for depth d are row n - 1 + d of drafter_table[b] (n = tokens committed so
+ * far; row g holds the logits for stream position g, clamped to the table),
+ * and the TARGET's greedy token at a tree slot is golden[b][n + depth] when
+ * the slot's path from the root follows golden[b], else V-1 (and V-1 at
+ * padding slots); the target's logits row is 1 there and 0 elsewhere. With
+ * such a target, autoregressive greedy decoding yields golden[b] itself.
+ * The projections the verify step attends with are fixed inputs (q_lat,
+ * q_pe, kv_new), the same every step. */
+typedef struct ddt_loop_args {
+  ddt_tree_dims tree; /* B, D, K, budget, V */
+  ddt_attn_dims attn; /* B, Q = budget + 1, H, C, R, paging, dtype (also of both logits
+                         tables), kv_rows, scale; max_len bounds prefix_len0 + n_new +
+                         budget + 1 over the batch */
+  double theta;       /* rotary base */
+  int32_t n_new;      /* tokens to add to each sequence after its first (>= 0) */
+  int32_t max_steps;  /* bound on the verify steps (>= 1) */
+  int32_t golden_len; /* G >= 2: length of every golden stream and drafter table */
+  const int32_t* golden;     /* [B][G] target stream; golden[b][0] is the first token */
+  const void* drafter_table; /* [B][G][V] drafter logits per stream position */
+  const void* q_lat;         /* [B][Q][H][C] */
+  const void* q_pe;          /* [B][Q][H][R], before rotation */
+  const void* kv_new;        /* [B][Q][C+R], rope part before rotation */
+  void* kv_cache;            /* [kv_rows][C+R], paged by block_table */
+  const int32_t* block_table;  /* [B][max_pages] */
+  const int32_t* prefix_len0;  /* [B] cache length before the first step */
+  int32_t* prefix_len;         /* [B] working cache length; the final length after */
+  int32_t* committed;          /* out [B][n_new + 1]: the first token, then the decoded ones */
+  int32_t* n_committed;        /* out [B] */
+  int32_t* steps;              /* out [B]: verify steps this sequence took */
+  int32_t* accepted;           /* out [B][max_steps]: tokens each step committed (before
+                                  cutting at n_new), 0 after the last */
+  int32_t* status;             /* out [B]: error bits of the step that stopped a sequence */
+  void* workspace;             /* ddt_loop_workspace_size bytes, 256-byte aligned */
+  size_t workspace_bytes;
+} ddt_loop_args;
+
+typedef struct ddt_loop ddt_loop; /* an instantiated loop graph */
+
+/* Bytes of workspace the loop needs (0 for invalid args). */
+size_t ddt_loop_workspace_size(const ddt_loop_args* args);
+
+/* Capture the loop body (every step's launches, with these pointers) into a
+ * graph and instantiate it. The step's host checks run here: their DDT_E*
+ * code is returned and nothing is kept. Device memory is not touched. */
+int ddt_loop_create(const ddt_loop_args* args, ddt_loop** loop);
+
+/* Reset the loop state (committed = the first golden token, cache length =
+ * prefix_len0, outputs cleared) and run the whole loop on `stream`. May be
+ * called repeatedly; calls on the same loop must not overlap. */
+int ddt_loop_launch(ddt_loop* loop, cudaStream_t stream);
+
+/* Free the graph (deferred by CUDA until a launch in flight completes). */
+int ddt_loop_destroy(ddt_loop* loop);
+
 /* Static text for a DDT_E* return code. */
 const char* ddt_strerror(int code);
 

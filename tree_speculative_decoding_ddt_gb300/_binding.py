@@ -56,6 +56,16 @@ class StepArgs(ctypes.Structure):
         ("workspace_bytes", ctypes.c_size_t)]
 
 
+class LoopArgs(ctypes.Structure):
+    _fields_ = [("tree", TreeDims), ("attn", AttnDims), ("theta", ctypes.c_double),
+                ("n_new", ctypes.c_int32), ("max_steps", ctypes.c_int32),
+                ("golden_len", ctypes.c_int32)] + [
+        (n, _P) for n in (
+            "golden", "drafter_table", "q_lat", "q_pe", "kv_new", "kv_cache", "block_table",
+            "prefix_len0", "prefix_len", "committed", "n_committed", "steps", "accepted",
+            "status", "workspace")] + [("workspace_bytes", ctypes.c_size_t)]
+
+
 #: every symbol the header declares, with (restype, argtypes)
 SIGNATURES = {
     "ddt_tree_build": (ctypes.c_int, [ctypes.POINTER(TreeDims)] + [_P] * 13),
@@ -74,6 +84,10 @@ SIGNATURES = {
     "ddt_drafter_topk": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
                                         ctypes.c_int, _P, _P, _P, _P]),
     "ddt_rope_append": (ctypes.c_int, [ctypes.POINTER(AttnDims), ctypes.c_double] + [_P] * 9),
+    "ddt_loop_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(LoopArgs)]),
+    "ddt_loop_create": (ctypes.c_int, [ctypes.POINTER(LoopArgs), ctypes.POINTER(_P)]),
+    "ddt_loop_launch": (ctypes.c_int, [_P, _P]),
+    "ddt_loop_destroy": (ctypes.c_int, [_P]),
     "ddt_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "ddt_abi_version": (ctypes.c_int, []),
 }
@@ -432,3 +446,90 @@ def ddt_step(buf: StepBuffers, stream=None):
     rc = load().ddt_step(ctypes.byref(buf.args), _stream(stream))
     _check("ddt_step", rc)
     return buf
+
+
+class DecodeLoop:
+    """The multi-step DDTree decode loop on the device (one CUDA graph with a
+    conditional WHILE node; see ``ddt_loop_create`` in the C header).
+
+    ``golden`` int32 [B, G] and ``drafter_table`` [B, G, V] stand in for the
+    target and the drafter; ``q_lat`` [B,Q,H,C], ``q_pe`` [B,Q,H,R] and
+    ``kv_new`` [B,Q,C+R] are the fixed projections each step attends with;
+    ``kv_cache`` [rows, C+R], ``block_table`` int32 [B, max_pages] and
+    ``prefix_len0`` int32 [B] describe the cache. All CUDA tensors of one
+    element type (float32 or bfloat16) except the int32 ones. Outputs live in
+    device tensors read by :meth:`results`."""
+
+    def __init__(self, golden, drafter_table, q_lat, q_pe, kv_new, kv_cache, block_table,
+                 prefix_len0, D: int, K: int, budget: int, n_new: int, max_steps: int,
+                 page_size: int, scale: float, max_len: int, theta: float = 10000.0):
+        B, G = golden.shape
+        V = int(drafter_table.shape[-1])
+        Q = budget + 1
+        dt = q_lat.dtype
+        if dt not in (torch.float32, torch.bfloat16):
+            raise TypeError("q_lat must be float32 or bfloat16")
+        H, C = q_lat.shape[2], q_lat.shape[3]
+        R = q_pe.shape[-1]
+        _need(golden, "golden", torch.int32, (B, G))
+        _need(drafter_table, "drafter_table", dt, (B, G, V))
+        _need(q_lat, "q_lat", dt, (B, Q, H, C))
+        _need(q_pe, "q_pe", dt, (B, Q, H, R))
+        _need(kv_new, "kv_new", dt, (B, Q, C + R))
+        _need(kv_cache, "kv_cache", dt)
+        _need(block_table, "block_table", torch.int32)
+        _need(prefix_len0, "prefix_len0", torch.int32, (B,))
+        dev = q_lat.device
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.prefix_len = torch.empty((B,), **i32)
+        self.committed = torch.empty((B, n_new + 1), **i32)
+        self.n_committed = torch.empty((B,), **i32)
+        self.steps = torch.empty((B,), **i32)
+        self.accepted = torch.empty((B, max_steps), **i32)
+        self.status = torch.empty((B,), **i32)
+        self._keep = (golden, drafter_table, q_lat, q_pe, kv_new, kv_cache, block_table,
+                      prefix_len0)
+        a = LoopArgs()
+        a.tree = TreeDims(B, D, K, budget, V)
+        a.attn = attn_dims(B, Q, H, C, R, page_size, block_table.shape[1], kv_cache.shape[0],
+                           DDT_F32 if dt == torch.float32 else DDT_BF16, scale, max_len)
+        a.theta, a.n_new, a.max_steps, a.golden_len = float(theta), n_new, max_steps, G
+        for name, tsr in (("golden", golden), ("drafter_table", drafter_table), ("q_lat", q_lat),
+                          ("q_pe", q_pe), ("kv_new", kv_new), ("kv_cache", kv_cache),
+                          ("block_table", block_table), ("prefix_len0", prefix_len0),
+                          ("prefix_len", self.prefix_len), ("committed", self.committed),
+                          ("n_committed", self.n_committed), ("steps", self.steps),
+                          ("accepted", self.accepted), ("status", self.status)):
+            setattr(a, name, tsr.data_ptr())
+        ws = int(load().ddt_loop_workspace_size(ctypes.byref(a)))
+        if ws == 0:
+            raise DdtError("ddt_loop_workspace_size", -1, "invalid loop arguments")
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+        a.workspace, a.workspace_bytes = self.workspace.data_ptr(), ws
+        self.args = a
+        h = _P()
+        _check("ddt_loop_create", load().ddt_loop_create(ctypes.byref(a), ctypes.byref(h)))
+        self._h = h
+
+    def launch(self, stream=None):
+        """Run the whole loop on ``stream`` (asynchronously)."""
+        if self._h is None:
+            raise RuntimeError("loop destroyed")
+        _check("ddt_loop_launch", load().ddt_loop_launch(self._h, _stream(stream)))
+
+    def results(self) -> dict:
+        """Host copies of the loop's outputs (synchronises)."""
+        torch.cuda.synchronize()
+        return {k: getattr(self, k).cpu().numpy() for k in
+                ("committed", "n_committed", "steps", "accepted", "status", "prefix_len")}
+
+    def close(self):
+        if getattr(self, "_h", None) is not None:
+            load().ddt_loop_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
