@@ -376,6 +376,67 @@ def time_next_rows(w, dev, stream, flush, n: int, buf=None) -> dict:
     return out
 
 
+def time_decode_loop(w, dev, stream, flush, n_new: int = 256, runs: int = 5) -> dict:
+    """The device decode loop (one CUDA graph, a conditional WHILE node over
+    whole verify steps) on this workload's shapes: B sequences, the drafter
+    hitting the stream at the workload's match rate, n_new tokens each.
+    Drafter table and stream drawn on the device; the committed tokens are
+    checked against the stream (DDTree == autoregressive output)."""
+    import torch
+    from tree_speculative_decoding_ddt_gb300 import _binding as DB
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4321)
+    ldt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    B, Q, G = w.B, w.Q, n_new + w.D + 1
+    golden = torch.randint(0, w.V - 1, (B, G), generator=gen, device=dev, dtype=torch.int32)
+    table = torch.randn((B, G, w.V), generator=gen, device=dev).to(ldt)
+    lo, hi = (w.match_p, w.match_p) if not isinstance(w.match_p, tuple) else w.match_p
+    rate = torch.linspace(lo, hi, B, device=dev)[:, None]
+    hit = torch.rand((B, G), generator=gen, device=dev) < rate
+    spike = table.float().amax(dim=-1) + 8.0
+    cur = table.gather(2, golden[..., None].long())[..., 0].float()
+    table.scatter_(2, golden[..., None].long(), torch.where(hit, spike, cur)[..., None].to(ldt))
+    lens = torch.full((B,), 4096 if not isinstance(w.prefix, int) else w.prefix,
+                      dtype=torch.int32, device=dev)
+    ps = 64
+    cap = int(lens.max()) + n_new + Q
+    pages = -(-cap // ps)
+    bt = torch.arange(B * pages, dtype=torch.int32, device=dev).reshape(B, pages)
+    kv = torch.randn((B * pages * ps, w.C + w.R), generator=gen, device=dev).to(ldt)
+    q_lat = torch.randn((B, Q, w.H, w.C), generator=gen, device=dev).to(ldt)
+    q_pe = torch.randn((B, Q, w.H, w.R), generator=gen, device=dev).to(ldt)
+    kv_new = torch.randn((B, Q, w.C + w.R), generator=gen, device=dev).to(ldt)
+    loop = DB.DecodeLoop(golden, table, q_lat, q_pe, kv_new, kv, bt, lens, D=w.D, K=w.K,
+                         budget=w.budget, n_new=n_new, max_steps=n_new, page_size=ps,
+                         scale=w.scale, max_len=cap)
+    loop.launch(stream)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(runs):
+        flush.fill_(1)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        loop.launch(stream)
+        e.record(stream)
+        ts.append((s, e))
+    torch.cuda.synchronize()
+    sec = statistics.median([s.elapsed_time(e) for s, e in ts]) / 1e3
+    res = loop.results()
+    ok = bool((res["committed"] == golden[:, : n_new + 1].cpu().numpy()).all())
+    steps = int(res["steps"].max())
+    made = int(res["accepted"].sum())
+    loop.close()
+    if not ok or (res["status"] != 0).any():
+        raise SystemExit("decode loop: committed tokens differ from the stream")
+    return {"graph": "one CUDA graph, conditional WHILE node over whole verify steps",
+            "B": B, "n_new": n_new, "drafter_hit_rate": [lo, hi], "us": sec * 1e6,
+            "tokens_per_s": B * n_new / sec, "verify_steps": steps,
+            "tokens_per_step": made / max(int(res["steps"].sum()), 1),
+            "us_per_step": sec * 1e6 / max(steps, 1), "ar_target_steps": n_new,
+            "greedy_exact": ok,
+            "data": "seeded device stream and drafter table; fixed synthetic projections"}
+
+
 def run_ours(args):
     import torch
     from tree_speculative_decoding_ddt_gb300 import _binding as DB
@@ -480,6 +541,8 @@ def run_ours(args):
         attn_ms = [s.elapsed_time(e) for s, e in aevs]
         # the next rows of the path, on this workload's shapes, timed the same way
         next_rows = time_next_rows(w, dev, stream, flush, n_attn, buf)
+        next_rows["decode_loop"] = time_decode_loop(w, dev, stream, flush,
+                                                    n_new=max(16, min(256, 4096 // w.B)))
     clocks = clk.summary()
 
     # end to end through the public API: host inputs in pinned memory are
