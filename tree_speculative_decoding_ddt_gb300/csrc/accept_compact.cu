@@ -32,6 +32,9 @@ __global__ void __launch_bounds__(kThreads) k_accept_compact(AcceptCompactArgs a
   __shared__ int32_t s_status;
   __shared__ int32_t s_target[kMaxQ];
 
+  // a kernel launched as this one's programmatic dependent (the split-KV
+  // merge of the same step) needs nothing from it: let it start now
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const int lane = tid & 31;

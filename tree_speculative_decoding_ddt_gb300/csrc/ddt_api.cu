@@ -277,36 +277,6 @@ int ddt_step(const ddt_step_args* a, cudaStream_t stream) {
                        a->workspace_bytes);
   if (rc) return rc;
 
-  const int64_t De = a->tree.D < a->tree.budget ? a->tree.D : a->tree.budget;
-  const int64_t Ke = a->tree.K < a->tree.budget ? a->tree.K : a->tree.budget;
-  if (a->attn.dtype == DDT_BF16 && De * Ke <= ddt::kFuseMaxCand) {
-    // A inside B: the attention kernel builds the tree in a spare warp while
-    // its prefix tiles run; status starts from zero and is OR-ed
-    if (cudaMemsetAsync(a->status, 0, sizeof(int32_t) * (size_t)a->attn.B, stream) != cudaSuccess)
-      return DDT_ELAUNCH;
-    ddt::TreeFuse f{};
-    f.D = a->tree.D; f.K = a->tree.K; f.budget = a->tree.budget; f.V = a->tree.V;
-    f.topk_logp = a->topk_logp; f.topk_ids = a->topk_ids; f.root_tok = a->root_tok;
-    f.tokens = a->tokens; f.parents = a->parents; f.depths = a->depths;
-    f.vis_bits = a->vis_bits; f.vis = a->vis; f.first_child = a->first_child;
-    f.next_sibling = a->next_sibling; f.n_nodes = a->n_nodes;
-    rc = launched(ddt::launch_verify_attn_bf16(a->attn, a->q_lat, a->q_pe, a->kv_cache,
-                                               a->block_table, a->prefix_len, a->vis_bits,
-                                               a->out, a->lse, a->status, a->workspace,
-                                               a->workspace_bytes, stream, &f));
-    if (rc) return rc;
-  } else {
-    // A. build (overwrites status)
-    if (ddt::launch_tree_build(a->tree, a->topk_logp, a->topk_ids, a->root_tok, a->tokens,
-                               a->parents, a->depths, a->vis_bits, a->vis, a->first_child,
-                               a->next_sibling, a->n_nodes, a->status, stream) != cudaSuccess)
-      return DDT_ELAUNCH;
-    // B. verify attention over the tree just built
-    rc = run_attn(&a->attn, a->q_lat, a->q_pe, a->kv_cache, a->block_table, a->prefix_len,
-                  a->vis_bits, a->out, a->lse, a->status, a->workspace, a->workspace_bytes,
-                  stream);
-    if (rc) return rc;
-  }
   // C + D. accept and compaction in one kernel
   ddt::AcceptCompactArgs c{};
   c.B = a->attn.B; c.Q = a->attn.Q; c.D = a->tree.D;
@@ -318,6 +288,36 @@ int ddt_step(const ddt_step_args* a, cudaStream_t stream) {
   c.kv_rows = a->attn.kv_rows; c.kv = static_cast<uint8_t*>(a->kv_cache);
   c.block_table = a->block_table; c.prefix_len = a->prefix_len; c.new_len = a->new_len;
   c.status = a->status;
+
+  const int64_t De = a->tree.D < a->tree.budget ? a->tree.D : a->tree.budget;
+  const int64_t Ke = a->tree.K < a->tree.budget ? a->tree.K : a->tree.budget;
+  if (a->attn.dtype == DDT_BF16 && De * Ke <= ddt::kFuseMaxCand) {
+    // A inside B: the attention kernel builds the tree in a spare warp while
+    // its prefix tiles run; status starts from zero and is OR-ed. C + D are
+    // launched by the attention call, before its split-KV merge, which then
+    // runs beside them
+    if (cudaMemsetAsync(a->status, 0, sizeof(int32_t) * (size_t)a->attn.B, stream) != cudaSuccess)
+      return DDT_ELAUNCH;
+    ddt::TreeFuse f{};
+    f.D = a->tree.D; f.K = a->tree.K; f.budget = a->tree.budget; f.V = a->tree.V;
+    f.topk_logp = a->topk_logp; f.topk_ids = a->topk_ids; f.root_tok = a->root_tok;
+    f.tokens = a->tokens; f.parents = a->parents; f.depths = a->depths;
+    f.vis_bits = a->vis_bits; f.vis = a->vis; f.first_child = a->first_child;
+    f.next_sibling = a->next_sibling; f.n_nodes = a->n_nodes;
+    return launched(ddt::launch_verify_attn_bf16(a->attn, a->q_lat, a->q_pe, a->kv_cache,
+                                                 a->block_table, a->prefix_len, a->vis_bits,
+                                                 a->out, a->lse, a->status, a->workspace,
+                                                 a->workspace_bytes, stream, &f, &c));
+  }
+  // A. build (overwrites status)
+  if (ddt::launch_tree_build(a->tree, a->topk_logp, a->topk_ids, a->root_tok, a->tokens,
+                             a->parents, a->depths, a->vis_bits, a->vis, a->first_child,
+                             a->next_sibling, a->n_nodes, a->status, stream) != cudaSuccess)
+    return DDT_ELAUNCH;
+  // B. verify attention over the tree just built
+  rc = run_attn(&a->attn, a->q_lat, a->q_pe, a->kv_cache, a->block_table, a->prefix_len,
+                a->vis_bits, a->out, a->lse, a->status, a->workspace, a->workspace_bytes, stream);
+  if (rc) return rc;
   return launched(ddt::launch_accept_compact(c, stream));
 }
 

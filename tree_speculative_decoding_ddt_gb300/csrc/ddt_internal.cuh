@@ -80,7 +80,8 @@ cudaError_t launch_verify_attn_bf16(const ddt_attn_dims& d, const void* q_lat, c
                                     const int32_t* prefix_len, const uint64_t* vis_bits,
                                     void* out, float* lse, int32_t* status, void* workspace,
                                     size_t workspace_bytes, cudaStream_t stream,
-                                    const TreeFuse* fuse = nullptr);
+                                    const TreeFuse* fuse = nullptr,
+                                    const AcceptCompactArgs* then = nullptr);
 
 // The 256-row form of the bf16 verify attention (verify_attn_pair.cu): four-CTA
 // clusters, MMAs on paired SMs. `part_o` (bf16) / `part_lse` hold the split-KV

@@ -873,14 +873,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // w_s = exp(lse_s - max lse); one warp per query row, 16 columns per lane.
 // The partials are bf16 (each already normalised by its own sum), which
 // halves their round trip through memory; the merge runs in fp32.
-__global__ void __launch_bounds__(256) k_combine(long long total_rows, int n_split,
-                                                 const __nv_bfloat16* __restrict__ part_o,
-                                                 const float* __restrict__ part_lse,
-                                                 __nv_bfloat16* __restrict__ out,
-                                                 float* __restrict__ lse_out) {
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+__device__ void combine_row(long long row, long long total_rows, int n_split,
+                            const __nv_bfloat16* __restrict__ part_o,
+                            const float* __restrict__ part_lse, __nv_bfloat16* __restrict__ out,
+                            float* __restrict__ lse_out) {
   const int lane = threadIdx.x & 31;
-  if (row >= total_rows) return;
   float m = -INFINITY;
   for (int s = 0; s < n_split; ++s) m = fmaxf(m, part_lse[(long long)s * total_rows + row]);
   float acc[16];
@@ -918,6 +915,21 @@ __global__ void __launch_bounds__(256) k_combine(long long total_rows, int n_spl
                         pack_bf16(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv),
                         pack_bf16(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv));
   if (lse_out && lane == 0) lse_out[row] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
+}
+
+// Split-KV merge: one warp per query row. Launched as the programmatic
+// dependent of the step's accept + compaction kernel, it runs beside it and
+// then waits for it before exiting, so work queued after the merge still
+// finds the step complete (without such a predecessor the wait returns at
+// once).
+__global__ void __launch_bounds__(256) k_combine(long long total_rows, int n_split,
+                                                 const __nv_bfloat16* __restrict__ part_o,
+                                                 const float* __restrict__ part_lse,
+                                                 __nv_bfloat16* __restrict__ out,
+                                                 float* __restrict__ lse_out) {
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row < total_rows) combine_row(row, total_rows, n_split, part_o, part_lse, out, lse_out);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- host side
@@ -1081,7 +1093,7 @@ cudaError_t launch_verify_attn_bf16(const ddt_attn_dims& d, const void* q_lat, c
                                     const int32_t* prefix_len, const uint64_t* vis_bits,
                                     void* out, float* lse, int32_t* status, void* workspace,
                                     size_t workspace_bytes, cudaStream_t stream,
-                                    const TreeFuse* fuse) {
+                                    const TreeFuse* fuse, const AcceptCompactArgs* then) {
   const Plan pl = choose_plan(d);
   const long long rows = (long long)d.B * d.Q * d.H;
   if (d.kv_rows < 1 || rows > 0x7fffffffLL || d.kv_rows > 0x7fffffffLL)
@@ -1126,10 +1138,33 @@ cudaError_t launch_verify_attn_bf16(const ddt_attn_dims& d, const void* q_lat, c
         tm_s, tm_o, tm_ql, tm_qp, p);
     e = cudaGetLastError();
   }
-  if (e != cudaSuccess || pl.n_split == 1) return e;
-  k_combine<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(rows, pl.n_split, part_o, part_lse,
-                                                            static_cast<__nv_bfloat16*>(out), lse);
-  return cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (pl.n_split == 1) return then != nullptr ? launch_accept_compact(*then, stream) : e;
+  if (then == nullptr) {
+    k_combine<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
+        rows, pl.n_split, part_o, part_lse, static_cast<__nv_bfloat16*>(out), lse);
+    return cudaGetLastError();
+  }
+  // accept + compaction first (it needs the tree and the finished cache
+  // reads of the attention, not its output), then the merge as its
+  // programmatic dependent: k_accept_compact lets dependents start at once,
+  // and the merge's inputs come from the attention, which completed before
+  // k_accept_compact began, so the two run side by side
+  e = launch_accept_compact(*then, stream);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((rows + 7) / 8), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_combine, rows, pl.n_split,
+                            static_cast<const __nv_bfloat16*>(part_o),
+                            static_cast<const float*>(part_lse), static_cast<__nv_bfloat16*>(out),
+                            lse);
 }
 
 int verify_attn_bf16_rows_per_tile(const ddt_attn_dims& d) { return choose_plan(d).rows; }
