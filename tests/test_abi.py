@@ -68,3 +68,22 @@ def test_host_side_argument_errors(lib):
     d = B.attn_dims(1, 9, 64, 256, 64, 64, 1, 100, B.DDT_BF16, 0.1, 100)
     assert lib.ddt_verify_attn_workspace_size(ctypes.byref(d)) == 0  # C=256 unsupported on bf16
     assert lib.ddt_step(None, None) == -1
+
+
+def test_host_side_errors_of_the_next_rows(lib):
+    # no pointer is dereferenced and nothing is launched: every call is
+    # refused on the host
+    assert lib.ddt_target_argmax(0, 10, B.DDT_BF16, None, None, None) == -1
+    assert lib.ddt_drafter_topk(4, 10, 17, B.DDT_BF16, 1, 1, 1, None) == -2
+    assert lib.ddt_drafter_topk(4, 10, 11, B.DDT_BF16, 1, 1, 1, None) == -2  # K > V
+    dims = B.attn_dims(1, 2, 1, 8, 7, 4, 1, 8, B.DDT_BF16, 1.0, 0)       # odd R
+    assert lib.ddt_rope_append(ctypes.byref(dims), 10000.0, *([1] * 8), None) == -1
+    dims = B.attn_dims(1, 2, 1, 8, 8, 4, 1, 8, B.DDT_BF16, 1.0, 0)
+    assert lib.ddt_rope_append(ctypes.byref(dims), 0.0, *([1] * 8), None) == -1
+    assert lib.ddt_rope_append(ctypes.byref(dims), 10000.0, None, *([1] * 7), None) == -1
+    a = B.LoopArgs()
+    assert lib.ddt_loop_workspace_size(ctypes.byref(a)) == 0
+    h = ctypes.c_void_p()
+    assert lib.ddt_loop_create(ctypes.byref(a), ctypes.byref(h)) == -1 and not h.value
+    assert lib.ddt_loop_launch(None, None) == -1
+    assert lib.ddt_loop_destroy(None) == 0
