@@ -39,7 +39,6 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxCluster = 8;
 constexpr int kMaxK = 16;
-constexpr int kInFlight = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float ex2f(float x) {
@@ -241,8 +240,14 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
   return v;
 }
 
-template <typename T, int KT>
-__global__ void __launch_bounds__(kThreads)
+// kIF: 16-byte loads a thread issues before using any. Three launch shapes:
+// rows that fill more than three CTAs per SM take 6 loads in flight and at
+// most 64 registers (K <= 8), so four CTAs fit per SM and the grid runs as
+// one wave; small shares (up to 32 vectors a thread) take 16 with two CTAs
+// per SM, so one or two batches cover them and a cluster of eight still
+// finds room; the rest take 8 with three CTAs per SM.
+template <typename T, int KT, int kIF, int kMinBlocks>
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
     k_drafter_topk(const T* __restrict__ logits, long long V, int K, int vec,
                    float* __restrict__ topk_logp, int32_t* __restrict__ topk_ids) {
   using E = Elems<T>;
@@ -271,10 +276,10 @@ __global__ void __launch_bounds__(kThreads)
   if (vec) {
     const long long nv = (c1 - c0) / E::kPerVec;
     const uint4* xv = reinterpret_cast<const uint4*>(x + c0);
-    for (long long base = 0; base < nv; base += (long long)kThreads * kInFlight) {
-      uint4 v[kInFlight];
+    for (long long base = 0; base < nv; base += (long long)kThreads * kIF) {
+      uint4 v[kIF];
 #pragma unroll
-      for (int k = 0; k < kInFlight; ++k) {
+      for (int k = 0; k < kIF; ++k) {
         const long long i = base + tid + (long long)k * kThreads;
         if (i < nv) v[k] = ld_stream(xv + i);
       }
@@ -284,7 +289,7 @@ __global__ void __launch_bounds__(kThreads)
         // K-th value from below and spares the lanes most first inserts
         float lm = -INFINITY;
 #pragma unroll
-        for (int k = 0; k < kInFlight; ++k) {
+        for (int k = 0; k < kIF; ++k) {
           if (base + tid + (long long)k * kThreads >= nv) continue;
           float f[E::kPerVec];
           E::unpack(v[k], f);
@@ -294,7 +299,7 @@ __global__ void __launch_bounds__(kThreads)
         wthr = warp_kth_value(lm, K);
       }
 #pragma unroll
-      for (int k = 0; k < kInFlight; ++k) {
+      for (int k = 0; k < kIF; ++k) {
         const long long i = base + tid + (long long)k * kThreads;
         if (i >= nv) continue;
         float f[E::kPerVec];
@@ -432,17 +437,30 @@ cudaError_t launch_drafter_topk(long long rows, long long V, int K, int dtype, c
   const int vb = aligned && V % 8 == 0, vf = aligned && V % 4 == 0;
   const __nv_bfloat16* lb = static_cast<const __nv_bfloat16*>(logits);
   const float* lf = static_cast<const float*>(logits);
-#define DDT_TOPK_LAUNCH(KT)                                                                      \
-  return dtype == DDT_BF16                                                                       \
-             ? launch_row_kernel(k_drafter_topk<__nv_bfloat16, KT>, rows, kMaxCluster,      \
-                                 kThreads, stream, lb, V, K, vb, topk_logp, topk_ids)            \
-             : launch_row_kernel(k_drafter_topk<float, KT>, rows, kMaxCluster, kThreads,      \
-                                 stream, lf, V, K, vf, topk_logp, topk_ids);
+  // the launch shape (see k_drafter_topk)
+  const int sms = device_sm_count();
+  const unsigned csize = row_cluster_size(rows, kMaxCluster);
+  const long long per_thread =
+      ((V + csize - 1) / csize + 8LL * kThreads - 1) / (8LL * kThreads);  // bf16 vectors
+  const int shape = rows * csize > 3LL * sms ? 0 : (per_thread <= 32 ? 1 : 2);
+#define DDT_TOPK_SHAPE(KT, IF, MB)                                                            \
+  return dtype == DDT_BF16                                                                    \
+             ? launch_row_kernel(k_drafter_topk<__nv_bfloat16, KT, IF, MB>, rows, kMaxCluster, \
+                                 kThreads, stream, lb, V, K, vb, topk_logp, topk_ids)         \
+             : launch_row_kernel(k_drafter_topk<float, KT, IF, MB>, rows, kMaxCluster,         \
+                                 kThreads, stream, lf, V, K, vf, topk_logp, topk_ids);
+#define DDT_TOPK_LAUNCH(KT)                 \
+  {                                         \
+    if (shape == 0) DDT_TOPK_SHAPE(KT, 6, (KT >= 16 ? 2 : 4)) \
+    if (shape == 1) DDT_TOPK_SHAPE(KT, 16, 2) \
+    DDT_TOPK_SHAPE(KT, 8, (KT >= 16 ? 2 : 3)) \
+  }
   if (K <= 1) DDT_TOPK_LAUNCH(1)
   if (K <= 2) DDT_TOPK_LAUNCH(2)
   if (K <= 4) DDT_TOPK_LAUNCH(4)
   if (K <= 8) DDT_TOPK_LAUNCH(8)
   DDT_TOPK_LAUNCH(16)
+#undef DDT_TOPK_SHAPE
 #undef DDT_TOPK_LAUNCH
 }
 
