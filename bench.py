@@ -379,6 +379,87 @@ def time_next_rows(w, dev, stream, flush, n: int, buf=None) -> dict:
     return out
 
 
+def _stage_rows(B, D, K, Q, C, R, elem, kv, block_table, page_size, prefix_len, topk_logp,
+                topk_ids, root_tok, target, budget, V, stream, flush, n) -> dict:
+    """Event-timed tree build, accept and compaction calls (L2 flushed before
+    each), each with its algorithmic bytes and achieved GB/s against the
+    measured HBM copy bandwidth."""
+    import torch
+    from tree_speculative_decoding_ddt_gb300 import _binding as DB
+    hbm, _, src = measured_peaks()
+    dev = topk_logp.device
+    W = (Q + 63) // 64
+    tree = DB.ddt_tree_build(topk_logp, topk_ids, root_tok, budget, V)
+    st = torch.zeros((B,), dtype=torch.int32, device=dev)
+    t_build = _event_median_s(lambda: DB.ddt_tree_build(topk_logp, topk_ids, root_tok, budget, V,
+                                                        out=tree), stream, flush, n)
+    acc = DB.ddt_tree_accept(tree["tokens"], tree["parents"], target, D, status=st)
+    t_acc = _event_median_s(lambda: DB.ddt_tree_accept(tree["tokens"], tree["parents"], target,
+                                                       D, status=st), stream, flush, n)
+    t_cmp = _event_median_s(lambda: DB.ddt_cache_compact(kv, block_table, prefix_len,
+                                                         acc["accept_idx"], acc["accept_len"],
+                                                         page_size, status=st), stream, flush, n)
+    moved = int(acc["accept_len"].sum())
+    out = {}
+    for name, sec, byt, kern in (
+            ("tree_build", t_build, B * D * K * 8 + B * Q * (12 + 8 * W + 8), "k_tree_build"),
+            ("accept", t_acc, B * Q * 12 + B * (D + 1) * 8, "k_accept_compact (accept only)"),
+            ("compact", t_cmp, 2 * moved * (C + R) * elem, "k_accept_compact (gather only)")):
+        out[name] = {"kernel": kern, "us": sec * 1e6, "algorithmic_bytes": byt,
+                     "achieved": byt / sec / 1e9, "unit": "GB/s", "peak": hbm,
+                     "frac": byt / sec / 1e9 / hbm, "peak_source": src}
+    out["compact"]["rows_moved"] = moved
+    return out
+
+
+def time_stages(w, buf, dev, stream, flush, n: int) -> dict:
+    """Build, accept and compaction of this workload's step, each timed alone
+    (they move kilobytes, so latency sets their time; µs is the figure)."""
+    elem = buf.q_pe.element_size()
+    # the compaction moves rows inside the tree slots of the step's cache,
+    # which the e2e leg rewrites before every step
+    return _stage_rows(w.B, w.D, w.K, w.Q, w.C, w.R, elem, buf.kv_cache, buf.block_table,
+                       buf.attn.page_size, buf.prefix_len, buf.topk_logp, buf.topk_ids,
+                       buf.root_tok, buf.target_argmax, w.budget, w.V, stream, flush, n)
+
+
+def time_stress(dev, stream, flush, n: int, B: int = 65536) -> dict:
+    """An addition to the workloads: B = 65536 sequences with the batched
+    workload's drafter shape (c3: D 8, K 4, budget 16, V 163840, bf16 cache
+    rows of 576), so that build, accept and compaction move
+    megabytes and bandwidth becomes the meaningful figure. The rank-0
+    candidate of every depth is boosted far ahead of the others and the target
+    agrees with it, so each tree's rank-0 chain is popped first and accepted in
+    full (accept_len = min(D, budget)); the cache holds 16 prefix slots and
+    the tree slots of every sequence, one page each."""
+    import torch
+    from tree_speculative_decoding_ddt_gb300 import workloads as WL
+    w = WL.CONFIGS["c3"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(99)
+    D, K, budget, V = w.D, w.K, w.budget, w.V
+    Q = budget + 1
+    logp = -torch.rand((B, D, K), generator=gen, device=dev) * 4.0 - 30.0
+    logp[:, :, 0] = -0.01
+    logp = logp.sort(dim=-1, descending=True).values.contiguous()
+    ids = torch.randint(0, V, (B, D, K), generator=gen, device=dev, dtype=torch.int32)
+    root = torch.randint(0, V, (B,), generator=gen, device=dev, dtype=torch.int32)
+    target = torch.zeros((B, Q), dtype=torch.int32, device=dev)
+    ne = min(D, budget)
+    target[:, :ne] = ids[:, :ne, 0]  # slot s < ne is the rank-0 chain node at depth s
+    page = 16 + Q
+    page = -(-page // 64) * 64
+    kv = torch.zeros((B * page, w.C + w.R), dtype=torch.bfloat16 if w.dtype == "bf16"
+                     else torch.float32, device=dev)
+    bt = torch.arange(B, dtype=torch.int32, device=dev).reshape(B, 1)
+    L = torch.full((B,), 16, dtype=torch.int32, device=dev)
+    out = _stage_rows(B, D, K, Q, w.C, w.R, kv.element_size(), kv, bt, page, L, logp, ids,
+                      root, target, budget, V, stream, flush, n)
+    out["note"] = (f"addition: B={B} sequences, drafter D={D} K={K} budget={budget}, "
+                   f"rank-0 chain accepted in full, seeded device inputs")
+    return out
+
+
 def time_decode_loop(w, dev, stream, flush, n_new: int = 256, runs: int = 5) -> dict:
     """The device decode loop (one CUDA graph, a conditional WHILE node over
     whole verify steps) on this workload's shapes: B sequences, the drafter
@@ -546,6 +627,8 @@ def run_ours(args):
         next_rows = time_next_rows(w, dev, stream, flush, n_attn, buf)
         next_rows["decode_loop"] = time_decode_loop(w, dev, stream, flush,
                                                     n_new=max(16, min(256, 4096 // w.B)))
+        stages = time_stages(w, buf, dev, stream, flush, n_attn)
+        stages["stress"] = time_stress(dev, stream, flush, n_attn)
     clocks = clk.summary()
 
     # end to end through the public API: host inputs in pinned memory are
@@ -733,6 +816,7 @@ def run_ours(args):
                            "compute; the host reads every step's results") if use_graph else
                           "direct calls, then a host synchronize every step"},
         "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms)},
+        "stages": stages,
         "next": next_rows,
     }
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
