@@ -97,3 +97,41 @@ def test_compaction_range_errors():
     idx = np.array([[0, 2, -1], [0, 1, 2], [0, 7, -1], [0, -4, -1]])
     n = np.array([1, 2, 1, 1])
     compact_both(kv, bt, L, idx, n, 16)
+
+
+def test_many_sequences_share_a_cta():
+    # past two sequences per SM a CTA serves up to eight sequences (one warp
+    # walks each); trees of mixed shape with and without a matching path,
+    # then compaction of all of them, against the oracle bit for bit
+    g = np.random.default_rng(17)
+    B, Q, D = 1000, 17, 8
+    parents = np.array([[-1] + [int(g.integers(0, c)) for c in range(1, Q)] for _ in range(B)])
+    tokens = g.integers(0, 3, (B, Q))
+    target = g.integers(0, 3, (B, Q))
+    ref = accept_both(tokens, parents, target, D)
+    assert ref["accept_len"].max() >= 3
+    P, width = 8, 72
+    pages_per = -(-(40 + Q) // P)
+    kv = g.integers(0, 60000, (B * pages_per * P, width)).astype(np.uint16)
+    bt = g.permutation(B * pages_per).reshape(B, pages_per).astype(np.int32)
+    L = g.integers(0, 40, B)
+    L[::97] = pages_per * P  # a few sequences out of range
+    compact_both(kv, bt, L, np.asarray(ref["accept_idx"]), np.asarray(ref["accept_len"]), P)
+
+
+def test_many_sequences_given_paths():
+    # the compaction-only branch on a large batch: given accepted paths,
+    # several sequences per CTA
+    g = np.random.default_rng(23)
+    B, D = 700, 5
+    P, width = 16, 40
+    pages_per = 4
+    kv = g.integers(0, 60000, (B * pages_per * P, width)).astype(np.uint16)
+    bt = g.permutation(B * pages_per).reshape(B, pages_per).astype(np.int32)
+    L = g.integers(0, 30, B)
+    n = g.integers(0, D + 1, B)
+    idx = np.full((B, D + 1), -1)
+    for b in range(B):
+        idx[b, 0] = 0
+        idx[b, 1: n[b] + 1] = np.sort(g.choice(np.arange(1, 20), n[b], replace=False))
+    compact_both(kv, bt, L, idx, n, P)

@@ -13,51 +13,67 @@
 // the whole CTA and only then written, so a source slot that is also a
 // later destination slot is read before it is overwritten.
 //
-// One CTA per sequence. Warp 0 walks the tree: every lane holds four tree
-// slots in registers, one ballot per 32 slots finds the lowest-slot child
-// whose token matches the target argmax. Then all threads move 16-byte
-// chunks.
+// A CTA serves up to eight sequences (one per warp; one per CTA when the
+// batch is small, so every thread helps with one sequence's rows). A warp
+// walks its tree: every lane holds four tree slots in registers, one ballot
+// per 32 slots finds the lowest-slot child whose token matches the target
+// argmax. Then all threads of the CTA move the accepted rows of all its
+// sequences in 16-byte chunks: every row into shared memory, a barrier, every
+// row out.
 #include "ddt_internal.cuh"
 
 namespace ddt {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
 constexpr int kSlotsPerLane = kMaxQ / 32;
 
-__global__ void __launch_bounds__(kThreads) k_accept_compact(AcceptCompactArgs a) {
+// seqs: sequences per CTA (1..kWarps); sequence blockIdx.x * seqs + w is
+// walked by warp w. The dynamic shared memory holds seqs x D rows.
+__global__ void __launch_bounds__(kThreads) k_accept_compact(AcceptCompactArgs a, int seqs) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  __shared__ int32_t s_path[kMaxQ + 1];
-  __shared__ int32_t s_len;
-  __shared__ int32_t s_status;
-  __shared__ int32_t s_target[kMaxQ];
+  __shared__ int32_t s_path[kWarps][kMaxQ + 1];
+  __shared__ int32_t s_len[kWarps];
+  __shared__ int32_t s_status[kWarps];
+  __shared__ int32_t s_ok[kWarps];
 
   // a kernel launched as this one's programmatic dependent (the split-KV
   // merge of the same step) needs nothing from it: let it start now
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const int D = a.D;
+  const int Q = a.Q;
+  const long long b0 = (long long)blockIdx.x * seqs;
 
-  if (a.do_accept) {
-    const int Q = a.Q;
-    for (int c = tid; c < Q; c += kThreads) s_target[c] = a.target[(size_t)b * Q + c];
-    __syncthreads();
-    if (warp == 0) {
-      int32_t tok[kSlotsPerLane], par[kSlotsPerLane];
+  if (warp < seqs) {
+    const long long b = b0 + warp;
+    if (b >= a.B) {
+      if (lane == 0) s_len[warp] = -1;
+    } else if (a.do_accept) {
+      int32_t tok[kSlotsPerLane], par[kSlotsPerLane], tgt[kSlotsPerLane];
 #pragma unroll
       for (int k = 0; k < kSlotsPerLane; ++k) {
         const int c = lane + 32 * k;
-        tok[k] = c < Q ? a.tokens[(size_t)b * Q + c] : 0;
-        par[k] = c < Q ? a.parents[(size_t)b * Q + c] : -2;
+        tok[k] = c < Q ? a.tokens[b * Q + c] : 0;
+        par[k] = c < Q ? a.parents[b * Q + c] : -2;
+        tgt[k] = c < Q ? a.target[b * Q + c] : 0;
       }
+      // target argmax at slot c, from the lane that holds it
+      auto target_at = [&](int c) -> int32_t {
+        int32_t v = tgt[0];
+#pragma unroll
+        for (int k = 1; k < kSlotsPerLane; ++k)
+          if ((c >> 5) == k) v = tgt[k];
+        return __shfl_sync(0xffffffffu, v, c & 31);
+      };
       unsigned long long visited_lo = 1ull, visited_hi = 0ull;  // slot 0 (root) is on the path
       int cur = 0, len = 0, st = 0;
-      if (lane == 0) s_path[0] = 0;
+      if (lane == 0) s_path[warp][0] = 0;
       for (int hop = 0; hop < D; ++hop) {
-        const int32_t want = s_target[cur];
+        const int32_t want = target_at(cur);
         int nxt = -1;
 #pragma unroll
         for (int k = 0; k < kSlotsPerLane; ++k) {
@@ -73,90 +89,134 @@ __global__ void __launch_bounds__(kThreads) k_accept_compact(AcceptCompactArgs a
         if (nxt < 64) visited_lo |= bit;
         else visited_hi |= bit;
         ++len;
-        if (lane == 0) s_path[len] = nxt;
+        if (lane == 0) s_path[warp][len] = nxt;
         cur = nxt;
       }
+      const int32_t bonus = target_at(cur);
       __syncwarp();
-      const int32_t bonus = s_target[cur];
-      int32_t* idx_o = a.accept_idx + (size_t)b * (D + 1);
-      int32_t* tok_o = a.out_tokens + (size_t)b * (D + 1);
+      int32_t* idx_o = a.accept_idx + b * (D + 1);
+      int32_t* tok_o = a.out_tokens + b * (D + 1);
       for (int d = lane; d <= D; d += 32) {
-        const int slot = d <= len ? s_path[d] : -1;
+        const int slot = d <= len ? s_path[warp][d] : -1;
         idx_o[d] = slot;
         int32_t t = -1;
-        if (d < len) t = a.tokens[(size_t)b * Q + s_path[d + 1]];
+        if (d < len) t = a.tokens[b * Q + s_path[warp][d + 1]];
         else if (d == len) t = bonus;
         tok_o[d] = t;
       }
       if (lane == 0) {
         a.accept_len[b] = len;
         a.bonus[b] = bonus;
-        s_len = len;
-        s_status = st;
+        s_len[warp] = len;
+        s_status[warp] = st;
       }
+    } else {
+      const int len = a.accept_len[b];
+      if (lane == 0) {
+        s_len[warp] = len;
+        s_status[warp] = 0;
+      }
+      for (int d = lane; d <= D && d <= len && len >= 0; d += 32)
+        s_path[warp][d] = a.accept_idx[b * (D + 1) + d];
     }
-    __syncthreads();
-  } else {
-    if (tid == 0) {
-      int len = a.accept_len[b];
-      s_len = len;
-      s_status = 0;
-    }
-    __syncthreads();
-    const int len = s_len;
-    for (int d = tid; d <= D && d <= len && len >= 0; d += kThreads)
-      s_path[d] = a.accept_idx[(size_t)b * (D + 1) + d];
-    __syncthreads();
   }
+  __syncthreads();
 
-  if (a.do_compact) {
-    const int len = s_len;
-    const int64_t L = a.prefix_len[b];
-    const int64_t cap = (int64_t)a.max_pages * a.page_size;
-    const int32_t* bt = a.block_table + (size_t)b * a.max_pages;
-    // validity of the whole path (identical decision in every thread)
-    bool bad = len < 0 || len > D || L < 0 || L + len >= cap;
-    if (!bad) {
-      for (int d = 1; d <= len; ++d) {
-        const int64_t i = s_path[d];
-        if (i < 0 || L + i >= cap) bad = true;
+  if (!a.do_compact) {
+    if (warp < seqs && lane == 0 && b0 + warp < a.B) a.status[b0 + warp] |= s_status[warp];
+    return;
+  }
+  // validity of every path (warp w decides for its sequence)
+  if (warp < seqs) {
+    const long long b = b0 + warp;
+    const int len = s_len[warp];
+    bool bad = true;
+    if (b < a.B) {
+      const int64_t L = a.prefix_len[b];
+      const int64_t cap = (int64_t)a.max_pages * a.page_size;
+      const int32_t* bt = a.block_table + b * a.max_pages;
+      bad = len < 0 || len > D || L < 0 || L + len >= cap;
+      if (!bad) {
+        for (int d = 1 + lane; d <= len; d += 32) {
+          const int64_t i = s_path[warp][d];
+          if (i < 0 || L + i >= cap) bad = true;
+        }
+        bad = __any_sync(0xffffffffu, bad);
       }
-    }
-    if (!bad) {
-      for (int d = tid; d < 2 * len; d += kThreads) {
-        const int64_t slot = d < len ? L + s_path[d + 1] : L + (d - len) + 1;
-        const int64_t row = slot_row(bt, a.page_size, slot);
-        if (row < 0 || row >= a.kv_rows) bad = true;
+      if (!bad) {
+        for (int d = lane; d < 2 * len; d += 32) {
+          const int64_t slot = d < len ? L + s_path[warp][d + 1] : L + (d - len) + 1;
+          const int64_t row = slot_row(bt, a.page_size, slot);
+          if (row < 0 || row >= a.kv_rows) bad = true;
+        }
+        bad = __any_sync(0xffffffffu, bad);
       }
-      bad = __syncthreads_or(bad);
-    }
-    if (bad) {
-      if (tid == 0) {
-        a.new_len[b] = (int32_t)L;
-        a.status[b] |= s_status | DDT_ST_RANGE;
+      if (lane == 0) {
+        if (bad) {
+          a.new_len[b] = (int32_t)L;
+          a.status[b] |= s_status[warp] | DDT_ST_RANGE;
+        }
+        s_ok[warp] = !bad;
       }
-      return;
+    } else if (lane == 0) {
+      s_ok[warp] = 0;
     }
-    const int chunks_per_row = a.row_bytes / 16;
-    const int total = len * chunks_per_row;
-    uint4* buf = reinterpret_cast<uint4*>(smem_raw);
-    for (int e = tid; e < total; e += kThreads) {
-      const int d = e / chunks_per_row + 1, ch = e % chunks_per_row;
-      const int64_t row = slot_row(bt, a.page_size, L + s_path[d]);
-      buf[e] = reinterpret_cast<const uint4*>(a.kv + row * a.row_bytes)[ch];
+  }
+  __syncthreads();
+  // every accepted row of the CTA's sequences into shared memory, then out:
+  // one flat range of 16-byte chunks over all of them, so every thread keeps
+  // several loads in flight whatever the sequences' lengths
+  const int chunks_per_row = a.row_bytes / 16;
+  int off[kWarps + 1];  // first chunk of each sequence in the flat range
+  off[0] = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w)
+    off[w + 1] = off[w] + ((w < seqs && s_ok[w]) ? s_len[w] * chunks_per_row : 0);
+  const int total = off[kWarps];
+  uint4* buf = reinterpret_cast<uint4*>(smem_raw);
+  auto locate = [&](int e, int& w, int& d, int& ch) {
+    w = 0;
+#pragma unroll
+    for (int k = 1; k < kWarps; ++k)
+      if (e >= off[k]) w = k;
+    const int r = e - off[w];
+    d = r / chunks_per_row + 1;
+    ch = r % chunks_per_row;
+  };
+  constexpr int kBatch = 4;  // loads a thread issues before storing any
+  for (int e0 = tid; e0 < total; e0 += kThreads * kBatch) {
+    uint4 v[kBatch];
+    size_t at[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int e = e0 + k * kThreads;
+      if (e >= total) break;
+      int w, d, ch;
+      locate(e, w, d, ch);
+      const long long b = b0 + w;
+      const int64_t row = slot_row(a.block_table + b * a.max_pages, a.page_size,
+                                   (int64_t)a.prefix_len[b] + s_path[w][d]);
+      v[k] = reinterpret_cast<const uint4*>(a.kv + row * a.row_bytes)[ch];
+      at[k] = (size_t)w * D * chunks_per_row + (size_t)(d - 1) * chunks_per_row + ch;
     }
-    __syncthreads();
-    for (int e = tid; e < total; e += kThreads) {
-      const int d = e / chunks_per_row + 1, ch = e % chunks_per_row;
-      const int64_t row = slot_row(bt, a.page_size, L + d);
-      reinterpret_cast<uint4*>(a.kv + row * a.row_bytes)[ch] = buf[e];
-    }
-    if (tid == 0) {
-      a.new_len[b] = (int32_t)(L + 1 + len);
-      a.status[b] |= s_status;
-    }
-  } else if (tid == 0) {
-    a.status[b] |= s_status;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k)
+      if (e0 + k * kThreads < total) buf[at[k]] = v[k];
+  }
+  __syncthreads();
+  for (int e = tid; e < total; e += kThreads) {
+    int w, d, ch;
+    locate(e, w, d, ch);
+    const long long b = b0 + w;
+    const int64_t row = slot_row(a.block_table + b * a.max_pages, a.page_size,
+                                 (int64_t)a.prefix_len[b] + d);
+    reinterpret_cast<uint4*>(a.kv + row * a.row_bytes)[ch] =
+        buf[(size_t)w * D * chunks_per_row + (size_t)(d - 1) * chunks_per_row + ch];
+  }
+  if (tid < seqs && s_ok[tid]) {
+    const long long b = b0 + tid;
+    a.new_len[b] = (int32_t)(a.prefix_len[b] + 1 + s_len[tid]);
+    a.status[b] |= s_status[tid];
   }
 }
 
@@ -167,13 +227,23 @@ size_t accept_compact_smem_bytes(int32_t D, int32_t row_bytes) {
 }
 
 cudaError_t launch_accept_compact(const AcceptCompactArgs& a, cudaStream_t stream) {
-  const size_t smem = a.do_compact ? accept_compact_smem_bytes(a.D, a.row_bytes) : 0;
+  // sequences per CTA: one while the batch leaves SMs free (every thread then
+  // helps with that sequence's rows), up to eight (one per warp) beyond, as
+  // many as the rows' shared memory allows
+  const size_t per_seq = a.do_compact ? accept_compact_smem_bytes(a.D, a.row_bytes) : 0;
+  int seqs = 1;
+  if (a.B > 2LL * device_sm_count()) {
+    seqs = kWarps;
+    while (seqs > 1 && per_seq * (size_t)seqs > 200 * 1024) seqs /= 2;
+  }
+  const size_t smem = per_seq * (size_t)seqs;
   static int smem_set[64] = {};
-  if (smem > 48 * 1024) {
+  if (smem + sizeof(int32_t) * kWarps * (kMaxQ + 4) > 48 * 1024) {  // with the static arrays
     cudaError_t e = ensure_smem_limit(k_accept_compact, (int)smem, smem_set);
     if (e != cudaSuccess) return e;
   }
-  k_accept_compact<<<a.B, kThreads, smem, stream>>>(a);
+  const long long grid = (a.B + seqs - 1) / seqs;
+  k_accept_compact<<<(unsigned)grid, kThreads, smem, stream>>>(a, seqs);
   return cudaGetLastError();
 }
 
