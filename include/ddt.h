@@ -49,7 +49,7 @@ extern "C" {
 /* ---- host return codes ---------------------------------------------------- */
 #define DDT_OK 0
 #define DDT_EINVAL (-1)       /* invalid argument (null pointer, negative size, ...) */
-#define DDT_EUNSUPPORTED (-2) /* valid but outside what this build supports */
+#define DDT_EUNSUPPORTED (-2) /* valid but outside what this library supports */
 #define DDT_ELAUNCH (-3)      /* a CUDA launch or query failed */
 #define DDT_EWORKSPACE (-4)   /* workspace missing or smaller than required */
 

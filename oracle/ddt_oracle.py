@@ -42,7 +42,7 @@ Sources (page title, then section):
   best node and pushes its first child and its next sibling, ties break by
   lower depth then lower rank, construction stops at the token budget.
 
-Readings of points the sources leave open (each one is listed in the design doc):
+Readings of points the sources leave open:
 
 * heap key ``(-score, depth, rank, parent_index)``; the parent index is this
   library's extension and makes the order total;
