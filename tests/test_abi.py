@@ -87,3 +87,70 @@ def test_host_side_errors_of_the_next_rows(lib):
     assert lib.ddt_loop_create(ctypes.byref(a), ctypes.byref(h)) == -1 and not h.value
     assert lib.ddt_loop_launch(None, None) == -1
     assert lib.ddt_loop_destroy(None) == 0
+
+
+def test_struct_layouts_match_a_c_compiler():
+    """Every field offset and struct size of the binding's ctypes mirrors
+    equals what a C compiler lays out from include/ddt.h."""
+    import shutil
+    import subprocess
+    import tempfile
+    cc = shutil.which("gcc") or shutil.which("cc")
+    cuda_inc = os.environ.get("CUDA_HOME", "/usr/local/cuda") + "/include"
+    if cc is None or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime_api.h")):
+        pytest.skip("needs a C compiler and the CUDA headers")
+    structs = {"ddt_tree_dims": B.TreeDims, "ddt_attn_dims": B.AttnDims,
+               "ddt_step_args": B.StepArgs, "ddt_loop_args": B.LoopArgs}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "ddt.h"', 'int main(void) {']
+    for cname, py in structs.items():
+        lines.append(f'  printf("{cname} size %zu\\n", sizeof({cname}));')
+        for f in py._fields_:
+            lines.append(f'  printf("{cname} {f[0]} %zu\\n", offsetof({cname}, {f[0]}));')
+    lines += ['  return 0;', '}']
+    with tempfile.TemporaryDirectory() as d:
+        src, exe = os.path.join(d, "layout.c"), os.path.join(d, "layout")
+        open(src, "w").write("\n".join(lines) + "\n")
+        subprocess.run([cc, "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, src, "-o", exe],
+                       check=True, capture_output=True)
+        out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout.split("\n")
+    got = {}
+    for line in out:
+        if line:
+            cname, field, val = line.split()
+            got[(cname, field)] = int(val)
+    for cname, py in structs.items():
+        assert got[(cname, "size")] == ctypes.sizeof(py), cname
+        for f in py._fields_:
+            assert got[(cname, f[0])] == getattr(py, f[0]).offset, (cname, f[0])
+
+
+def test_loop_arguments_are_checked_on_the_host(lib):
+    # each case breaks one rule of ddt_loop_args; nothing reaches the GPU
+    def args(**kw):
+        a = B.LoopArgs()
+        a.tree = B.TreeDims(2, 4, 3, 8, 512)
+        a.attn = B.attn_dims(2, 9, 2, 16, 8, 64, 1, 256, B.DDT_F32, 0.25, 128)
+        a.theta, a.n_new, a.max_steps, a.golden_len = 10000.0, 12, 64, 20
+        for name, _ in B.LoopArgs._fields_[6:-1]:
+            setattr(a, name, 64)  # non-null, never dereferenced
+        for k, v in kw.items():
+            if k in ("B", "D", "K", "budget", "V"):
+                setattr(a.tree, k, v)
+            elif k in ("Q", "dtype"):
+                setattr(a.attn, k, v)
+            else:
+                setattr(a, k, v)
+        return a
+    assert lib.ddt_loop_workspace_size(ctypes.byref(args())) > 0
+    for bad in (dict(Q=10), dict(B=3), dict(D=0), dict(V=1), dict(n_new=-1),
+                dict(max_steps=0), dict(golden_len=1), dict(dtype=7), dict(golden=None),
+                dict(accepted=None)):
+        a = args(**bad)
+        assert lib.ddt_loop_workspace_size(ctypes.byref(a)) == 0, bad
+        h = ctypes.c_void_p()
+        assert lib.ddt_loop_create(ctypes.byref(a), ctypes.byref(h)) == -1, bad
+        assert not h.value
+    # valid arguments without a workspace are refused before any capture
+    h = ctypes.c_void_p()
+    assert lib.ddt_loop_create(ctypes.byref(args(workspace=None)), ctypes.byref(h)) == -4
+    assert not h.value
