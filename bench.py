@@ -95,8 +95,10 @@ MEASURED_TRAFFIC = {
     ("c4_deep_long", 256): ("verify_attn_pair.cu",
                             "1faffa2d2bd194e71e8c69231e6afb1e6b6b79b3d0bac158d15a7be7c562e30c",
                             884251648 + 38849792),
+    # captured with the file at sha 79b0bd59…; since then only k_combine and
+    # the host launcher in that file changed, k_verify_attn_bf16 itself not
     ("c3_batched_paged", 128): ("verify_attn_bf16.cu",
-                                "79b0bd59b655e27bb215965f48b6ac16293cd104f864987f8061f08566f3090d",
+                                "81b164da7a004cd7396d10eb949cc8fff33a7ccb455859d9b5e080d028f6f5f1",
                                 502247424 + 62564352),
 }
 
