@@ -283,8 +283,10 @@ typedef struct ddt_step_args {
 size_t ddt_step_workspace_size(const ddt_step_args* args);
 
 /* A -> B -> C+D on `stream`: tree build, verify attention, accept and
- * compaction (accept and compaction run fused in one kernel). status is
- * overwritten, then OR-ed by every stage. */
+ * compaction (accept and compaction run fused in one kernel; when B splits
+ * the key range, its merge pass runs beside C+D, which needs only the tree
+ * and B's finished cache reads). Everything enqueued after ddt_step sees the
+ * whole step done. status is overwritten, then OR-ed by every stage. */
 int ddt_step(const ddt_step_args* args, cudaStream_t stream);
 
 /* Target-side argmax at every tree slot: the target model's greedy token,
