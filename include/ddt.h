@@ -32,8 +32,10 @@
  *  - Integer arrays are int32, row-major, densely packed (strides in the
  *    comments). Nodes of a tree are numbered in the order the builder pops
  *    them: slot 0 is the root, and every node's parent has a lower slot.
- *  - Thread-compatible: calls on different streams may run concurrently; the
- *    library's only global state is a per-device cache of device properties.
+ *  - Thread-compatible: calls on different streams may run concurrently. The
+ *    library's global state is a per-device cache of device properties, plus
+ *    what ddt_verify_attn_noalloc needs: a 32 MiB device array reserved on
+ *    every GPU that loads the library, and a per-device cache of its address.
  */
 #ifndef DDT_H_
 #define DDT_H_
@@ -194,7 +196,9 @@ int ddt_verify_attn(const ddt_attn_dims* dims, const void* q_lat, const void* q_
  * DDT_EUNSUPPORTED for DDT_F32. All calls share the array: calls whose GPU
  * work may overlap (several streams or host threads) race and must be
  * serialised by the caller. The first call on a device looks up the array's
- * address with that device current; make it before any stream capture. */
+ * address with that device current and keeps it (first calls from several host
+ * threads at once are safe); make it before any stream capture, and do not
+ * use this entry point after a cudaDeviceReset of that device. */
 int ddt_verify_attn_noalloc(const ddt_attn_dims* dims, const void* q_lat, const void* q_pe,
                             const void* kv_cache, const int32_t* block_table,
                             const int32_t* prefix_len, const uint64_t* vis_bits, void* out,

@@ -154,3 +154,43 @@ def test_loop_arguments_are_checked_on_the_host(lib):
     h = ctypes.c_void_p()
     assert lib.ddt_loop_create(ctypes.byref(args(workspace=None)), ctypes.byref(h)) == -4
     assert not h.value
+
+
+def _cpu(shape, dtype=None):
+    import torch
+    return torch.zeros(shape, dtype=dtype or torch.bfloat16)
+
+
+@pytest.mark.parametrize("fn", ["ddt_verify_attn", "ddt_verify_attn_noalloc"])
+@pytest.mark.parametrize("kv_shape", [(256, 512), (256, 640), (4, 64, 576), (256,)])
+def test_attention_wrappers_refuse_a_malformed_cache_before_any_call(fn, kv_shape):
+    # The library views the cache as kv_rows rows of C+R elements; a cache of
+    # another shape would be read past its end, so the wrappers refuse it on
+    # the shapes alone (these CPU tensors never reach the library).
+    import torch
+    nb, Q, H, C, R = 1, 9, 4, 512, 64
+    args = (_cpu((nb, Q, H, C)), _cpu((nb, Q, H, R)), _cpu(kv_shape),
+            _cpu((nb, 4), torch.int32), _cpu((nb,), torch.int32), _cpu((nb, Q, 1), torch.int64))
+    with pytest.raises(ValueError, match="kv_cache"):
+        getattr(B, fn)(*args, 0.05, 64, 40)
+
+
+@pytest.mark.parametrize("fn", ["ddt_verify_attn", "ddt_verify_attn_noalloc"])
+def test_attention_wrappers_refuse_mismatched_tables(fn):
+    import torch
+    nb, Q, H, C, R = 2, 9, 4, 512, 64
+    good = dict(q_lat=_cpu((nb, Q, H, C)), q_pe=_cpu((nb, Q, H, R)), kv=_cpu((256, C + R)),
+                bt=_cpu((nb, 4), torch.int32), pl=_cpu((nb,), torch.int32),
+                vis=_cpu((nb, Q, 1), torch.int64))
+    for key, bad, what in (("bt", _cpu((1, 4), torch.int32), "block_table"),
+                           ("pl", _cpu((3,), torch.int32), "prefix_len"),
+                           ("vis", _cpu((nb, Q, 2), torch.int64), "vis_bits"),
+                           ("q_pe", _cpu((nb, Q, H + 1, R)), "q_pe")):
+        a = dict(good, **{key: bad})
+        with pytest.raises(ValueError, match=what):
+            getattr(B, fn)(a["q_lat"], a["q_pe"], a["kv"], a["bt"], a["pl"], a["vis"],
+                            0.05, 64, 40)
+    # well-shaped CPU tensors get past the shape checks and stop at the device check
+    with pytest.raises(TypeError, match="CUDA"):
+        getattr(B, fn)(*good.values(), 0.05, 64, 40)
+

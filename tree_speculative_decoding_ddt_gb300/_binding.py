@@ -138,6 +138,32 @@ def _need(t: torch.Tensor, name: str, dtype, shape=None):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
+def check_attn_shapes(q_lat, q_pe, kv_cache, block_table, prefix_len, vis_bits):
+    """Shape checks shared by the verify-attention wrappers, made before any
+    device check or library call: the library sizes its cache views from
+    (kv_rows, C + R), so a cache of any other shape would be read past its end.
+    Returns (B, Q, H, C, R)."""
+    if q_lat.dim() != 4:
+        raise ValueError(f"q_lat must be [B, Q, H, C], got {tuple(q_lat.shape)}")
+    B, Q, H, C = (int(x) for x in q_lat.shape)
+    if q_pe.dim() != 4 or tuple(q_pe.shape[:3]) != (B, Q, H):
+        raise ValueError(f"q_pe must be [B, Q, H, R] = [{B}, {Q}, {H}, R], "
+                         f"got {tuple(q_pe.shape)}")
+    R = int(q_pe.shape[3])
+    if kv_cache.dim() != 2 or int(kv_cache.shape[1]) != C + R:
+        raise ValueError(f"kv_cache must be [rows, C+R] = [rows, {C + R}], "
+                         f"got {tuple(kv_cache.shape)}")
+    if block_table.dim() != 2 or int(block_table.shape[0]) != B:
+        raise ValueError(f"block_table must be [B, max_pages] with B = {B}, "
+                         f"got {tuple(block_table.shape)}")
+    if tuple(prefix_len.shape) != (B,):
+        raise ValueError(f"prefix_len must be [{B}], got {tuple(prefix_len.shape)}")
+    W = (Q + 63) // 64
+    if tuple(vis_bits.shape) != (B, Q, W):
+        raise ValueError(f"vis_bits must be [{B}, {Q}, {W}], got {tuple(vis_bits.shape)}")
+    return B, Q, H, C, R
+
+
 def ddt_tree_build(topk_logp: torch.Tensor, topk_ids: torch.Tensor, root_tok: torch.Tensor,
                    budget: int, V: int, with_vis: bool = False, out: Optional[dict] = None,
                    stream=None) -> dict:
@@ -196,8 +222,7 @@ def ddt_verify_attn(q_lat, q_pe, kv_cache, block_table, prefix_len, vis_bits, sc
     [B,Q,H,R], ``kv_cache`` [rows, C+R] (float32 or bfloat16), ``block_table``
     int32 [B,max_pages], ``prefix_len`` int32 [B], ``vis_bits`` int64 [B,Q,W].
     Returns (out, lse, status)."""
-    B, Q, H, C = q_lat.shape
-    R = q_pe.shape[-1]
+    B, Q, H, C, R = check_attn_shapes(q_lat, q_pe, kv_cache, block_table, prefix_len, vis_bits)
     dt = q_lat.dtype
     if dt not in (torch.float32, torch.bfloat16):
         raise TypeError("q_lat must be float32 or bfloat16")
@@ -205,8 +230,6 @@ def ddt_verify_attn(q_lat, q_pe, kv_cache, block_table, prefix_len, vis_bits, sc
     _need(q_lat, "q_lat", dt)
     _need(q_pe, "q_pe", dt, (B, Q, H, R))
     _need(kv_cache, "kv_cache", dt)
-    if kv_cache.dim() != 2 or kv_cache.shape[1] != C + R:
-        raise ValueError("kv_cache must be [rows, C+R]")
     _need(block_table, "block_table", torch.int32)
     _need(prefix_len, "prefix_len", torch.int32, (B,))
     _need(vis_bits, "vis_bits", torch.int64, (B, Q, (Q + 63) // 64))
@@ -238,8 +261,7 @@ def ddt_verify_attn_noalloc(q_lat, q_pe, kv_cache, block_table, prefix_len, vis_
     from the library's fixed device array instead of a caller workspace, for
     callers that cannot allocate device memory. Calls that may overlap on the
     GPU share that array and must be serialised. Returns (out, lse, status)."""
-    B, Q, H, C = q_lat.shape
-    R = q_pe.shape[-1]
+    B, Q, H, C, R = check_attn_shapes(q_lat, q_pe, kv_cache, block_table, prefix_len, vis_bits)
     _need(q_lat, "q_lat", torch.bfloat16)
     _need(q_pe, "q_pe", torch.bfloat16, (B, Q, H, R))
     _need(kv_cache, "kv_cache", torch.bfloat16)
@@ -353,6 +375,8 @@ def ddt_rope_append(q_pe, kv_new, kv_cache, block_table, prefix_len, depths, pag
     if kv_cache.dim() != 2 or kv_cache.shape[1] != CR:
         raise ValueError("kv_cache must be [rows, C+R]")
     _need(block_table, "block_table", torch.int32)
+    if block_table.dim() != 2 or int(block_table.shape[0]) != B:
+        raise ValueError(f"block_table must be [B, max_pages] with B = {B}")
     _need(prefix_len, "prefix_len", torch.int32, (B,))
     _need(depths, "depths", torch.int32, (B, Q))
     dev = q_pe.device
@@ -381,6 +405,8 @@ def ddt_cache_compact(kv_cache, block_table, prefix_len, accept_idx, accept_len,
     rows = kv_cache.shape[0]
     row_bytes = kv_cache[0].numel() * kv_cache.element_size() if rows else 0
     _need(block_table, "block_table", torch.int32)
+    if block_table.dim() != 2 or int(block_table.shape[0]) != B:
+        raise ValueError(f"block_table must be [B, max_pages] with B = {B}")
     _need(prefix_len, "prefix_len", torch.int32, (B,))
     _need(accept_idx, "accept_idx", torch.int32, (B, D + 1))
     _need(accept_len, "accept_len", torch.int32, (B,))
@@ -477,7 +503,12 @@ class DecodeLoop:
         _need(q_pe, "q_pe", dt, (B, Q, H, R))
         _need(kv_new, "kv_new", dt, (B, Q, C + R))
         _need(kv_cache, "kv_cache", dt)
+        if kv_cache.dim() != 2 or int(kv_cache.shape[1]) != C + R:
+            raise ValueError(f"kv_cache must be [rows, C+R] = [rows, {C + R}], "
+                             f"got {tuple(kv_cache.shape)}")
         _need(block_table, "block_table", torch.int32)
+        if block_table.dim() != 2 or int(block_table.shape[0]) != B:
+            raise ValueError(f"block_table must be [B, max_pages] with B = {B}")
         _need(prefix_len0, "prefix_len0", torch.int32, (B,))
         dev = q_lat.device
         i32 = dict(dtype=torch.int32, device=dev)

@@ -327,7 +327,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int sp_last = code ? 0 : (n_tiles - 1) / tps;
   const bool designated = p.fuse && rt == 0 && sp == sp_last;
   if (nt == 0) {
-    if (rank == 0 && tid == 0) mbar_wait(bar(B_Q_FULL), 0);  // nothing lands after exit
+    // nothing may land after exit: a Q load still pending when the bounded
+    // wait gives up is reported, as on the main path
+    if (rank == 0 && tid == 0 && !mbar_wait(bar(B_Q_FULL), 0)) atomicOr(p.status + b, DDT_ST_TIMEOUT);
     write_empty(p, b, rt, sp, rank);
     if (code && rt == 0 && sp == 0 && rank == 0 && tid == 0) atomicOr(p.status + b, code);
     if (designated && rank == 1 && warp == 6) {

@@ -18,10 +18,16 @@
 //  - every call uses the same array, so calls whose GPU work overlaps (other
 //    streams, other host threads) race on it; serialise them;
 //  - the first call on each device looks up the array's device address
-//    (cudaGetSymbolAddress, with that device current); make that first call
-//    before any stream capture;
+//    (cudaGetSymbolAddress, with that device current) and keeps it for the
+//    life of the process; make that first call before any stream capture.
+//    Host threads may make first calls at the same time (the address is kept
+//    in an atomic; racing lookups store the same value). A cudaDeviceReset
+//    destroys the array with the context, and the kept address then points at
+//    nothing: this entry point must not be used after a reset of its device;
 //  - nothing in the array needs to start at zero: every partial result the
 //    merge kernel reads is written earlier in the same call.
+#include <atomic>
+
 #include "ddt_internal.cuh"
 
 namespace {
@@ -31,16 +37,17 @@ constexpr size_t kScratchBytes = size_t(32) << 20;  // 32 MiB
 static __device__ __align__(256) unsigned char g_verify_scratch[kScratchBytes];
 
 // Device address of g_verify_scratch, looked up once per device.
-void* g_scratch_addr[64] = {};
+constexpr int kMaxDevices = 64;
+std::atomic<void*> g_scratch_addr[kMaxDevices];
 
 void* scratch_address(int device) {
-  if (device < 0 || device >= 64) return nullptr;
-  if (g_scratch_addr[device] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_verify_scratch) != cudaSuccess) return nullptr;
-    g_scratch_addr[device] = p;
+  if (device < 0 || device >= kMaxDevices) return nullptr;
+  void* p = g_scratch_addr[device].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    if (cudaGetSymbolAddress(&p, g_verify_scratch) != cudaSuccess || p == nullptr) return nullptr;
+    g_scratch_addr[device].store(p, std::memory_order_release);
   }
-  return g_scratch_addr[device];
+  return p;
 }
 
 }  // namespace

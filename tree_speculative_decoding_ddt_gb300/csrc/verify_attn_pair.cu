@@ -342,7 +342,9 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   const bool phantom = nt > 0 && j_begin + nt == n_tiles && 2 * n_tiles > n_blocks;
   const int n_msgs = 2 * nt - (phantom ? 1 : 0);
   if (nt == 0) {
-    if (s_side && tid == 0) mbar_wait(bar(B_Q_FULL), 0);  // nothing lands after exit
+    // nothing may land after exit: a Q load still pending when the bounded
+    // wait gives up is reported, as on the main path
+    if (s_side && tid == 0 && !mbar_wait(bar(B_Q_FULL), 0)) atomicOr(p.status + b, DDT_ST_TIMEOUT);
     write_empty(p, b, rt, sp, rank);
     if (code && rt == 0 && sp == 0 && rank == 0 && tid == 0) atomicOr(p.status + b, code);
     if (designated && rank == 2 && warp == 6) {
