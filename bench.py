@@ -3,12 +3,14 @@
 
 A step is the whole hot path through the C ABI (``ddt_step``): best-first
 tree build -> tree-verify MLA-absorb attention -> greedy accept + cache
-compaction, over one batch of the max-budget workload (B=1, D=16, K=8,
-budget 64 -> q_len 65, 64 heads, kv_lora 512, rope 64, prefix 4096, bf16).
-The step is captured in a CUDA graph and replayed; L2 is flushed (a 256 MiB
-write) between timed steps, outside the per-step CUDA events.
+compaction, over one batch of the deep-tree long-context workload by default
+(B=8, D=15, K=2, budget 64 -> q_len 65, 64 heads, kv_lora 512, rope 64,
+prefix 32768, bf16; every step accepts 15 drafts and compacts them), the
+largest fixed single-GPU configuration. The step is captured in a CUDA graph
+and replayed; L2 is flushed (a 256 MiB write) between timed steps, outside the
+per-step CUDA events.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c2]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c4]
     python bench.py --impl reference ...     # the CPU oracle as the reference arm
 
 Multi-GPU (torchrun, one process per GPU) runs independent replicas: the
@@ -45,7 +47,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="c2",
+    ap.add_argument("--config", default="c4",
                     help="c1..c4 or a sweep point q<len>_b<batch>_l<prefix>")
     ap.add_argument("--no-graph", action="store_true", help="launch each step directly")
     ap.add_argument("--cpu-seconds", type=float, default=20.0,
@@ -220,23 +222,55 @@ def barrier(world: int):
 
 # ------------------------------------------------------------- CPU oracle arm
 
-def oracle_steps(w, batch, seconds: float, max_steps: int):
-    """Time whole oracle steps (heapq build, float64 attention, accept,
-    compaction) until about ``seconds`` have passed; returns (steps, secs)."""
+def oracle_sequence(w, batch, b: int):
+    """The oracle's whole step (heapq build, float64 attention, accept,
+    compaction) on sequence ``b`` of the batch alone, as a callable. The
+    sequence's pages are gathered into a cache of its own beforehand, so the
+    timed call does exactly that sequence's share of the batch's work."""
     from oracle import ddt_oracle as O
     from tree_speculative_decoding_ddt_gb300 import workloads as WL
     lay = batch.layout
-    n = 0
-    t0 = time.perf_counter()
+    L = int(batch.prefix_len[b])
+    n_pages = -(-(L + w.Q) // lay.page_size)
+    kv = np.ascontiguousarray(batch.kv[lay.rows_of(b, np.arange(n_pages * lay.page_size))])
+    bt = np.arange(n_pages, dtype=np.int32).reshape(1, n_pages)
+    one = slice(b, b + 1)
+    p = float(batch.match_p[b])
+
+    def target(tree):
+        return WL.synth_target_argmax(tree["depths"][0], batch.topk_ids[b], batch.target_u[b],
+                                      batch.target_fallback[b], p)[None]
+
+    def run():
+        return O.ddt_step(batch.topk_logp[one], batch.topk_ids[one], batch.root_tok[one],
+                          w.budget, w.V, batch.q_lat[one], batch.q_pe[one], kv, bt,
+                          batch.prefix_len[one], w.scale, lay.page_size, n_pages, target)
+    return run
+
+
+def oracle_steps(w, batch, seconds: float, max_steps: int, first: int = 0):
+    """Time single-sequence oracle steps (sequences first, first+1, ... cycling
+    over the batch) until ``max_steps`` are done or about ``seconds`` have
+    passed (at least one). Returns (sequence steps, seconds, whole-batch
+    steps/s = 1 / (B x mean seconds per sequence))."""
+    n, secs = 0, 0.0
     while n < max_steps:
-        O.ddt_step(batch.topk_logp, batch.topk_ids, batch.root_tok, w.budget, w.V, batch.q_lat,
-                   batch.q_pe, batch.kv, lay.block_table, batch.prefix_len, w.scale,
-                   lay.page_size, lay.max_pages,
-                   lambda t: WL.target_argmax_for(batch, t["depths"]))
+        run = oracle_sequence(w, batch, (first + n) % w.B)
+        t0 = time.perf_counter()
+        run()
+        secs += time.perf_counter() - t0
         n += 1
-        if time.perf_counter() - t0 >= seconds:
+        if secs >= seconds:
             break
-    return n, time.perf_counter() - t0
+    return n, secs, n / (w.B * secs)
+
+
+def oracle_sample_text(w, n: int, model: str) -> str:
+    what = (f"{n} single-sequence oracle steps (python heapq build, numpy float64 attention, "
+            f"accept, compaction) of the workload on {model}")
+    if w.B == 1:
+        return what
+    return what + f"; whole-batch rate extrapolated as 1 / ({w.B} x mean seconds per sequence)"
 
 
 def cpu_info():
@@ -254,6 +288,10 @@ def cpu_info():
 
 
 def run_reference(args):
+    """The reference arm: the CPU oracle on the host cores, on the same
+    workload, metric and unit as the GPU arm. Each step is one sequence of the
+    batch (cycling), so a step stays a bounded sample; the whole-batch steps/s
+    is extrapolated by B."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
@@ -263,20 +301,19 @@ def run_reference(args):
     # W untimed warm-up steps, cut short after 30 s of them on a slow host
     warm, t_w = 0, time.perf_counter()
     while warm < args.warmup and time.perf_counter() - t_w < 30.0:
-        oracle_steps(w, batch, 0.0, 1)
+        oracle_sequence(w, batch, warm % w.B)()
         warm += 1
-    n, secs = oracle_steps(w, batch, args.cpu_seconds, max(1, args.steps))
+    # K timed steps, cut short after 150 s so the arm ends within minutes
+    n, secs, v = oracle_steps(w, batch, 150.0, max(1, args.steps), first=warm)
     cores, model = cpu_info()
-    v = n / secs
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": args.gpus,
-        "steps": n, "warmup": warm, "ms_per_step": 1e3 * secs / n,
+        "steps": n, "warmup": warm, "ms_per_step": 1e3 / v,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)",
         "config": {"workload": describe(w)},
         "cpu_baseline": {"value": v, "unit": "steps/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{n} whole oracle steps (python heapq build, numpy float64 "
-                                   f"attention, accept, compaction) on {model}"},
+                         "sample": oracle_sample_text(w, n, model)},
         "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -401,7 +438,13 @@ def _stage_rows(B, D, K, Q, C, R, elem, kv, block_table, page_size, prefix_len, 
     t_cmp = _event_median_s(lambda: DB.ddt_cache_compact(kv, block_table, prefix_len,
                                                          acc["accept_idx"], acc["accept_len"],
                                                          page_size, status=st), stream, flush, n)
-    moved = int(acc["accept_len"].sum())
+    # rows that really move: path slots not already in place
+    idx = acc["accept_idx"][:, 1:]
+    d = torch.arange(1, D + 1, device=dev, dtype=torch.int32)
+    inside = d[None, :] <= acc["accept_len"][:, None]
+    moved = int(((idx != d[None, :]) & inside).sum())
+    if int(st.abs().sum()) != 0:
+        raise SystemExit(f"stage timing: device status reports errors")
     out = {}
     for name, sec, byt, kern in (
             ("tree_build", t_build, B * D * K * 8 + B * Q * (12 + 8 * W + 8), "k_tree_build"),
@@ -428,37 +471,28 @@ def time_stages(w, buf, dev, stream, flush, n: int) -> dict:
 def time_stress(dev, stream, flush, n: int, B: int = 65536) -> dict:
     """An addition to the workloads: B = 65536 sequences with the batched
     workload's drafter shape (c3: D 8, K 4, budget 16, V 163840, bf16 cache
-    rows of 576), so that build, accept and compaction move
-    megabytes and bandwidth becomes the meaningful figure. The rank-0
-    candidate of every depth is boosted far ahead of the others and the target
-    agrees with it, so each tree's rank-0 chain is popped first and accepted in
-    full (accept_len = min(D, budget)); the cache holds 16 prefix slots and
-    the tree slots of every sequence, one page each."""
+    rows of 576), so that build, accept and compaction move megabytes and
+    bandwidth becomes the meaningful figure. The accepted path leaves the
+    rank-0 chain at the root (workloads.stress_inputs), so every sequence accepts 8
+    drafts and compaction really moves 8 rows; the cache holds 16 prefix slots
+    and the tree slots of every sequence, one page each."""
     import torch
     from tree_speculative_decoding_ddt_gb300 import workloads as WL
     w = WL.CONFIGS["c3"]
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(99)
     D, K, budget, V = w.D, w.K, w.budget, w.V
+    assert budget == 2 * D
     Q = budget + 1
-    logp = -torch.rand((B, D, K), generator=gen, device=dev) * 4.0 - 30.0
-    logp[:, :, 0] = -0.01
-    logp = logp.sort(dim=-1, descending=True).values.contiguous()
-    ids = torch.randint(0, V, (B, D, K), generator=gen, device=dev, dtype=torch.int32)
-    root = torch.randint(0, V, (B,), generator=gen, device=dev, dtype=torch.int32)
-    target = torch.zeros((B, Q), dtype=torch.int32, device=dev)
-    ne = min(D, budget)
-    target[:, :ne] = ids[:, :ne, 0]  # slot s < ne is the rank-0 chain node at depth s
-    page = 16 + Q
-    page = -(-page // 64) * 64
+    logp, ids, root, target = WL.stress_inputs(B, D, K, V, dev)
+    page = -(-(16 + Q) // 64) * 64
     kv = torch.zeros((B * page, w.C + w.R), dtype=torch.bfloat16 if w.dtype == "bf16"
                      else torch.float32, device=dev)
     bt = torch.arange(B, dtype=torch.int32, device=dev).reshape(B, 1)
     L = torch.full((B,), 16, dtype=torch.int32, device=dev)
     out = _stage_rows(B, D, K, Q, w.C, w.R, kv.element_size(), kv, bt, page, L, logp, ids,
                       root, target, budget, V, stream, flush, n)
-    out["note"] = (f"addition: B={B} sequences, drafter D={D} K={K} budget={budget}, "
-                   f"rank-0 chain accepted in full, seeded device inputs")
+    out["note"] = (f"addition: B={B} sequences, drafter D={D} K={K} budget={budget}; the "
+                   f"accepted path leaves the rank-0 chain at the root, {D} drafts accepted and "
+                   f"{D} rows moved per sequence; seeded device inputs")
     return out
 
 
@@ -634,78 +668,83 @@ def run_ours(args):
     clocks = clk.summary()
 
     # end to end through the public API: host inputs in pinned memory are
-    # copied in, the step runs, its result (accepted tokens, lengths, status)
-    # is copied out, every step
+    # copied in (the drafter's top-k, the queries with an unrotated rope part,
+    # the tree latents with an unrotated rope part, the target argmax), the
+    # tree is built, its rope parts are turned at positions L + depth and its
+    # latents appended to the cache (ddt_tree_build + ddt_rope_append), the
+    # step runs, and its result (accepted tokens, lengths, status) is copied
+    # out, every step
+    def pinned_lat(x):
+        x = np.ascontiguousarray(WL.to_bf16_bits(x).view(np.int16) if bf16 else x)
+        return torch.from_numpy(x).pin_memory()
+
     host_in = {
         "topk_logp": torch.from_numpy(batch.topk_logp).pin_memory(),
         "topk_ids": torch.from_numpy(batch.topk_ids).pin_memory(),
         "root_tok": torch.from_numpy(batch.root_tok).pin_memory(),
-        "q_lat": torch.from_numpy(np.ascontiguousarray(WL.to_bf16_bits(batch.q_lat).view(np.int16)
-                                                       if bf16 else batch.q_lat)).pin_memory(),
-        "q_pe": torch.from_numpy(np.ascontiguousarray(WL.to_bf16_bits(batch.q_pe).view(np.int16)
-                                                      if bf16 else batch.q_pe)).pin_memory(),
+        "q_lat": pinned_lat(batch.q_lat),
         "target_argmax": torch.from_numpy(WL.target_argmax_for(batch, depths)).pin_memory(),
     }
     tree_rows = np.concatenate([lay.rows_of(b, np.arange(int(batch.prefix_len[b]),
                                                          int(batch.prefix_len[b]) + w.Q))
                                 for b in range(w.B)])
-    tree_lat = batch.kv[tree_rows]
-    host_tree = torch.from_numpy(np.ascontiguousarray(
-        WL.to_bf16_bits(tree_lat).view(np.int16) if bf16 else tree_lat)).pin_memory()
-    tree_rows_dev = torch.from_numpy(tree_rows).to(dev)
-    tree_dev = torch.empty_like(host_tree, device=dev)
+    host_qpe = pinned_lat(batch.q_pe)
+    host_tree = pinned_lat(batch.kv[tree_rows].reshape(w.B, w.Q, w.C + w.R))
+    ldt = buf.q_pe.dtype
     outs = [buf.out_tokens, buf.accept_len, buf.new_len, buf.status]
     host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + \
-        host_tree.numel() * host_tree.element_size()
+        host_qpe.numel() * host_qpe.element_size() + host_tree.numel() * host_tree.element_size()
     d2h = sum(t.numel() * t.element_size() for t in outs)
-    kv_view = buf.kv_cache.view(torch.int16) if bf16 else buf.kv_cache
+    rope_status = torch.zeros((w.B,), dtype=torch.int32, device=dev)
 
-    def e2e_body():
+    def raw(t):  # bf16 device tensors take the host's int16 bit patterns
+        return t.view(torch.int16) if t.dtype == torch.bfloat16 else t
+
+    # Two input sets (set 0 is the step buffers' own): step i copies its
+    # inputs into set i % 2 on a copy stream while step i-1 still computes.
+    import types
+    in_names = list(host_in.keys())
+    sets = [{k: getattr(buf, k) for k in in_names + ["q_pe"]},
+            {k: getattr(buf, k).clone() for k in in_names + ["q_pe"]}]
+    qraw = [torch.empty_like(buf.q_pe) for _ in range(2)]
+    trees = [torch.empty((w.B, w.Q, w.C + w.R), dtype=ldt, device=dev) for _ in range(2)]
+    built = [DB.ddt_tree_build(sets[j]["topk_logp"], sets[j]["topk_ids"], sets[j]["root_tok"],
+                               w.budget, w.V) for j in range(2)]
+    a2 = DB.StepArgs.from_buffer_copy(buf.args)
+    for k in in_names + ["q_pe"]:
+        setattr(a2, k, sets[1][k].data_ptr())
+    step_of = [buf, types.SimpleNamespace(args=a2)]
+    houts = [host_out, [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]]
+
+    def copy_body(j):
         for k, h in host_in.items():
-            dst = getattr(buf, k)
-            (dst.view(torch.int16) if dst.dtype == torch.bfloat16 else dst).copy_(h, non_blocking=True)
-        tree_dev.copy_(host_tree, non_blocking=True)
-        kv_view.index_copy_(0, tree_rows_dev, tree_dev)  # cache append of the tree latents
-        DB.ddt_step(buf)
-        for h, t in zip(host_out, outs):
+            raw(sets[j][k]).copy_(h, non_blocking=True)
+        raw(qraw[j]).copy_(host_qpe, non_blocking=True)
+        raw(trees[j]).copy_(host_tree, non_blocking=True)
+
+    def comp_body(j):
+        tr = DB.ddt_tree_build(sets[j]["topk_logp"], sets[j]["topk_ids"], sets[j]["root_tok"],
+                               w.budget, w.V, out=built[j])
+        DB.ddt_rope_append(qraw[j], trees[j], buf.kv_cache, buf.block_table, buf.prefix_len,
+                           tr["depths"], lay.page_size, q_out=sets[j]["q_pe"],
+                           status=rope_status)
+        DB.ddt_step(step_of[j])
+        for h, t in zip(houts[j], outs):
             h.copy_(t, non_blocking=True)
 
     def e2e_step():
-        e2e_body()
+        copy_body(0)
+        comp_body(0)
         torch.cuda.current_stream().synchronize()
 
     if use_graph:
-        # Two input sets, two graphs each: step i copies its inputs into set
-        # i % 2 on a copy stream while step i-1 still computes; the compute
-        # graph (cache append, the step, results copied out) waits for its
-        # copy, the next copy into a set waits until the step that read it is
-        # done, and the host reads every step's results one step behind.
-        import types
-        in_names = list(host_in.keys())
-        sets = [{k: getattr(buf, k) for k in in_names},
-                {k: torch.empty_like(getattr(buf, k)) for k in in_names}]
-        trees = [tree_dev, torch.empty_like(tree_dev)]
-        a2 = DB.StepArgs.from_buffer_copy(buf.args)
-        for k in in_names:
-            setattr(a2, k, sets[1][k].data_ptr())
-        step_of = [buf, types.SimpleNamespace(args=a2)]
-        houts = [host_out, [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]]
+        # Two graphs per input set: the copies (on a copy stream) and the
+        # compute (build, rope + append, the step, results copied out). The
+        # compute graph waits for its copy, the next copy into a set waits
+        # until the step that read it is done, and the host reads every
+        # step's results one step behind.
         cstream, kstream = torch.cuda.Stream(), torch.cuda.current_stream()
-
-        def copy_body(j):
-            for k, h in host_in.items():
-                dst = sets[j][k]
-                (dst.view(torch.int16) if dst.dtype == torch.bfloat16 else dst).copy_(
-                    h, non_blocking=True)
-            trees[j].copy_(host_tree, non_blocking=True)
-
-        def comp_body(j):
-            kv_view.index_copy_(0, tree_rows_dev, trees[j])
-            DB.ddt_step(step_of[j])
-            for h, t in zip(houts[j], outs):
-                h.copy_(t, non_blocking=True)
-
         g_copy, g_comp = [], []
         for j in range(2):
             copy_body(j)
@@ -768,7 +807,7 @@ def run_ours(args):
             e2e_step()
         e2e_s = max(time.perf_counter() - t0, 1e-9)
 
-    st = buf.status.cpu().numpy()
+    st = buf.status.cpu().numpy() | rope_status.cpu().numpy()
     if (st & ~DB.ST_BUDGET_PAD).any():
         raise SystemExit(f"device status reports errors: {st}")
 
@@ -787,7 +826,8 @@ def run_ours(args):
         "steps": args.steps, "warmup": max(3, args.warmup),
         "ms_per_step": 1e3 * slowest / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded numpy generators)",
-        "config": {"workload": describe(w), "parallelism": f"replicas x{world}",
+        "config": {"workload": describe(w)},
+        "timing": {"parallelism": f"replicas x{world}",
                    "l2": "flushed by a 256 MiB write before every timed step, outside its events",
                    "launch": "cuda_graph replay" if use_graph else "direct C-ABI calls",
                    "bracket_s_incl_flush": bracket_s},
@@ -813,22 +853,21 @@ def run_ours(args):
                 "unit": "steps/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "launch": ("per step a copy graph (pinned host -> one of two device input "
-                           "sets, on a copy stream) and a compute graph (cache append, the "
-                           "step, results -> pinned host); step i's copy overlaps step i-1's "
-                           "compute; the host reads every step's results") if use_graph else
-                          "direct calls, then a host synchronize every step"},
+                           "sets, on a copy stream) and a compute graph (ddt_tree_build, "
+                           "ddt_rope_append of q_pe and the tree latents at positions L+depth "
+                           "into the cache, ddt_step, results -> pinned host); step i's copy "
+                           "overlaps step i-1's compute; the host reads every step's results")
+                          if use_graph else
+                          "the same calls issued directly, then a host synchronize every step"},
         "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms)},
         "stages": stages,
         "next": next_rows,
     }
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
-        n_cpu = max(1, int(args.cpu_seconds // 2))
-        n, secs = oracle_steps(w, batch, args.cpu_seconds, n_cpu * 50)
+        n, secs, v = oracle_steps(w, batch, args.cpu_seconds, 100000)
         cores, model = cpu_info()
-        line["cpu_baseline"] = {
-            "value": n / secs, "unit": "steps/s", "cores": cores, "kind": "oracle",
-            "sample": f"{n} whole oracle steps of the same workload (python heapq build, numpy "
-                      f"float64 attention, accept, compaction) on {model}"}
+        line["cpu_baseline"] = {"value": v, "unit": "steps/s", "cores": cores, "kind": "oracle",
+                                "sample": oracle_sample_text(w, n, model)}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

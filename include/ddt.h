@@ -235,10 +235,14 @@ int ddt_tree_accept(int32_t B, int32_t Q, int32_t D, const int32_t* tokens,
  * slot L + d (L = prefix_len[b]; the root stays at slot L), with every source
  * row read before any destination row is written. new_len[b] = L + 1 +
  * accept_len[b]. kv_cache is [kv_rows][row_bytes] bytes, paged as in
- * ddt_attn_dims. A sequence whose path or slots fall outside
- * [0, max_pages * page_size), or whose pages fall outside the kv_rows of the
- * cache, is left untouched, new_len = L, DDT_ST_RANGE.
- * Limits: row_bytes a positive multiple of 16, D * row_bytes <= 196608. */
+ * ddt_attn_dims. accept_idx[b][1..accept_len] must be a path from the root
+ * (slot 0) in pop order, as ddt_tree_accept writes it: strictly increasing,
+ * first entry >= 1 (accept_idx[b][0] is not read). Rows already in place
+ * (accept_idx[b][d] == d) are not touched. A sequence whose list is not such
+ * a path, whose slots fall outside [0, max_pages * page_size), or whose pages
+ * fall outside the kv_rows of the cache, is left untouched, new_len = L,
+ * DDT_ST_RANGE.
+ * Limits: row_bytes a positive multiple of 16, D <= DDT_MAX_Q - 1. */
 int ddt_cache_compact(int32_t B, int32_t D, int32_t row_bytes, int32_t page_size,
                       int32_t max_pages, int64_t kv_rows, void* kv_cache,
                       const int32_t* block_table,

@@ -330,6 +330,10 @@ def cache_compact(kv, block_table, prefix_len, accept_idx, accept_len, page_size
     copy), ``new_len = L + 1 + accept_len`` and per-sequence status. A
     sequence whose path or slots fall outside ``[0, max_pages * page_size)``,
     or whose pages fall outside ``kv``, is left untouched with ``ST_RANGE``.
+    So is one whose list is not a path from the root: nodes are numbered in
+    pop order and a parent pops before its child, so the slots of a path
+    increase strictly from the root's slot 0 (``accept_idx[0]`` is the root
+    and is not read).
     """
     new = np.array(kv, copy=True)
     B = len(prefix_len)
@@ -341,8 +345,10 @@ def cache_compact(kv, block_table, prefix_len, accept_idx, accept_len, page_size
         n = int(accept_len[b])
         D = accept_idx.shape[1] - 1
         src_slots = [L + int(accept_idx[b][d]) for d in range(1, n + 1)] if 0 <= n <= D else None
+        path = [0] + [int(accept_idx[b][d]) for d in range(1, n + 1)] if src_slots else [0]
         bad = (src_slots is None or L < 0 or L + n >= cap
                or any(int(accept_idx[b][d]) < 0 for d in range(1, n + 1))
+               or any(path[d] <= path[d - 1] for d in range(1, len(path)))
                or any(s >= cap for s in src_slots))
         if not bad:
             rows_used = slot_rows(block_table[b], page_size,

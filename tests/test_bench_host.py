@@ -71,3 +71,50 @@ def test_config_names_resolve():
     assert (w.Q, w.B, w.prefix) == (17, 8, 8192)
     with pytest.raises(SystemExit):
         bench.workload("nope")
+
+
+def test_single_sequence_oracle_step_is_that_sequences_share_of_the_batch_step():
+    # the CPU baselines time one sequence at a time (own cache of its pages)
+    # and extrapolate by B; each such step must do exactly what the batch
+    # step does for that sequence
+    w = WL.CONFIGS["c3"].with_(B=3, V=512, H=2, C=16, R=8, prefix=(40, 150))
+    batch = WL.make_batch(w)
+    lay = batch.layout
+    whole = O.ddt_step(batch.topk_logp, batch.topk_ids, batch.root_tok, w.budget, w.V,
+                       batch.q_lat, batch.q_pe, batch.kv, lay.block_table, batch.prefix_len,
+                       w.scale, lay.page_size, lay.max_pages,
+                       lambda t: WL.target_argmax_for(batch, t["depths"]))
+    for b in range(w.B):
+        one = bench.oracle_sequence(w, batch, b)()
+        for k in ("tokens", "parents", "depths", "vis_bits"):
+            np.testing.assert_array_equal(one["tree"][k][0], whole["tree"][k][b])
+        np.testing.assert_array_equal(one["o"][0], whole["o"][b])
+        for k in ("accept_idx", "accept_len", "out_tokens"):
+            np.testing.assert_array_equal(one["accept"][k][0], whole["accept"][k][b])
+        n = int(batch.prefix_len[b]) + w.Q
+        np.testing.assert_array_equal(one["kv"][:n], whole["kv"][lay.rows_of(b, np.arange(n))])
+        assert one["new_len"][0] == whole["new_len"][b]
+
+
+def test_oracle_steps_extrapolate_by_batch():
+    w = WL.CONFIGS["c1"].with_(B=4)
+    batch = WL.make_batch(w)
+    n, secs, v = bench.oracle_steps(w, batch, 0.0, 3)
+    assert n == 1 and v == pytest.approx(1.0 / (4 * secs))
+    n, secs, v = bench.oracle_steps(w, batch, 1e9, 5)
+    assert n == 5 and v == pytest.approx(5 / (4 * secs))
+
+
+def test_stress_point_accepts_a_path_off_the_rank0_chain():
+    # the stress point's drafter and target (drawn with torch, here on the
+    # CPU): the oracle accepts slots D+1 .. 2D, so every sequence moves D rows
+    import torch
+    D, K, V, B = 8, 4, 1000, 64
+    logp, ids, root, target = WL.stress_inputs(B, D, K, V, torch.device("cpu"))
+    tree = O.tree_build(logp.numpy(), ids.numpy(), root.numpy(), 2 * D, V)
+    acc = O.tree_accept(tree["tokens"], tree["parents"], target.numpy(), D)
+    assert (acc["accept_len"] == D).all()
+    for b in range(B):
+        assert list(tree["depths"][b][1: D + 1]) == list(range(1, D + 1))
+        assert list(acc["accept_idx"][b]) == [0] + list(range(D + 1, 2 * D + 1))
+        assert acc["accept_len"][b] == D

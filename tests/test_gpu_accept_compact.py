@@ -91,12 +91,41 @@ def test_compaction_paths_pages_and_overlaps(width, dt):
 
 
 def test_compaction_range_errors():
+    # past capacity, a page outside the cache, a negative slot, and lists that
+    # are not paths from the root (decreasing, repeated, the root itself)
     kv = np.arange(64 * 8, dtype=np.uint16).reshape(64, 8)
-    bt = np.array([[0, 1], [2, 3], [1, 9], [0, 1]], np.int32)
-    L = np.array([3, 28, 10, 4])
-    idx = np.array([[0, 2, -1], [0, 1, 2], [0, 7, -1], [0, -4, -1]])
-    n = np.array([1, 2, 1, 1])
+    bt = np.array([[0, 1], [2, 3], [1, 9], [0, 1], [0, 1], [2, 3], [1, 0], [3, 2]], np.int32)
+    L = np.array([3, 28, 10, 4, 2, 5, 7, 1])
+    idx = np.array([[0, 2, -1], [0, 1, 2], [0, 7, -1], [0, -4, -1], [0, 5, 3], [0, 4, 4],
+                    [0, 0, 3], [0, 1, 2]])
+    n = np.array([1, 2, 1, 1, 2, 2, 2, 2])
     compact_both(kv, bt, L, idx, n, 16)
+
+
+@pytest.mark.parametrize("B", [3, 700])
+def test_compaction_long_rows_with_overlaps_over_several_batches(B):
+    # rows of 4 KB, paths whose sources are also destinations, more chunks per
+    # CTA than one batch of loads holds: batches must follow increasing d
+    g = np.random.default_rng(B)
+    P, D, width = 8, 12, 2048
+    pages_per = 4
+    if B > 100:
+        width = 256  # 512 B rows, eight sequences per CTA
+    kv = g.integers(0, 60000, (B * pages_per * P, width)).astype(np.uint16)
+    bt = g.permutation(B * pages_per).reshape(B, pages_per).astype(np.int32)
+    L = g.integers(0, 6, B)
+    idx = np.full((B, D + 1), -1)
+    n = np.zeros(B, np.int64)
+    for b in range(B):
+        k = int(g.integers(0, D + 1))
+        if b % 3 == 0:  # dense: every source but the last is also a destination
+            path = list(range(2, k + 2))
+        else:
+            path = np.sort(g.choice(np.arange(1, 2 * D), k, replace=False))
+        idx[b, 0] = 0
+        idx[b, 1: k + 1] = path
+        n[b] = k
+    compact_both(kv, bt, L, idx, n, P)
 
 
 def test_many_sequences_share_a_cta():

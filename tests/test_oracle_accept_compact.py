@@ -143,7 +143,8 @@ def test_compaction_reads_before_writing_when_slots_overlap():
     assert new_len[0] == 7 and st[0] == 0
 
 
-@pytest.mark.parametrize("bad", ["neg_idx", "past_capacity", "len_too_long"])
+@pytest.mark.parametrize("bad", ["neg_idx", "past_capacity", "len_too_long", "decreasing",
+                                 "repeated", "root_as_child"])
 def test_compaction_range_errors_leave_sequence_untouched(bad):
     kv = _cache(16, 3, 1)
     bt = np.zeros((1, 1), np.int32)
@@ -154,8 +155,14 @@ def test_compaction_range_errors_leave_sequence_untouched(bad):
         idx[0, 2] = -1
     elif bad == "past_capacity":
         idx[0, 2] = 20
-    else:
+    elif bad == "len_too_long":
         n[0] = 3
+    elif bad == "decreasing":  # not a path: a child pops after its parent
+        idx[0, 1:] = [3, 2]
+    elif bad == "repeated":
+        idx[0, 1:] = [2, 2]
+    else:  # slot 0 is the root, never one of its own descendants
+        idx[0, 1:] = [0, 4]
     new, new_len, st = O.cache_compact(kv, bt, L, idx, n, 16, 1)
     assert st[0] == O.ST_RANGE and new_len[0] == 5
     np.testing.assert_array_equal(new, kv)
@@ -184,3 +191,27 @@ def test_compaction_page_outside_cache_is_a_range_error():
                                        8, 2)
     assert st[0] == O.ST_RANGE and new_len[0] == 6
     np.testing.assert_array_equal(new, kv)
+
+
+def test_accepted_paths_increase_strictly_from_the_root():
+    # the walk follows parent -> child edges and the builder numbers nodes in
+    # pop order (a parent pops before its children), so every accepted path
+    # is a valid compaction list: 0 = s_0 < s_1 < ... < s_len
+    g = np.random.default_rng(5)
+    for trial in range(40):
+        w = WL.CONFIGS["c1"].with_(B=4, D=int(g.integers(1, 6)), K=int(g.integers(1, 5)),
+                                   budget=int(g.integers(0, 20)), V=6)
+        batch = WL.make_batch(w, latents=False)
+        tree = O.tree_build(batch.topk_logp, batch.topk_ids, batch.root_tok, w.budget, w.V)
+        target = g.integers(0, w.V, (w.B, w.Q)).astype(np.int32)
+        # half the slots follow a child so that paths get long
+        for b in range(w.B):
+            for c in range(1, w.Q):
+                p = int(tree["parents"][b][c])
+                if p >= 0 and g.random() < 0.5:
+                    target[b][p] = tree["tokens"][b][c]
+        acc = O.tree_accept(tree["tokens"], tree["parents"], target, w.D)
+        for b in range(w.B):
+            n = int(acc["accept_len"][b])
+            path = [int(x) for x in acc["accept_idx"][b][: n + 1]]
+            assert path[0] == 0 and all(path[d] > path[d - 1] for d in range(1, n + 1))

@@ -9,17 +9,25 @@
 //
 // Compaction: "The Checkpoint", section "The Message" (cache append +
 // post-verify compaction; after accept, gather the accepted-path latents;
-// gather/copy rows). The accepted rows are first read into shared memory by
-// the whole CTA and only then written, so a source slot that is also a
-// later destination slot is read before it is overwritten.
+// gather/copy rows). Row d of the path (slot s_d, d = 1..len) moves to slot d.
+// Nodes are numbered in pop order, so a path from the root has strictly
+// increasing slots, 0 = s_0 < s_1 < ... < s_len, hence s_d >= d: rows with
+// s_d == d are already in place and are not touched, and for every moved row
+// s_d > d. A moved row's destination d is never the source of a later row
+// (those read slots s_d' >= d' > d), so rows copied in increasing d need no
+// staging; only when some source slot is also a destination (s_d <= len) do
+// the loads of a batch of rows wait at a barrier for all of them before the
+// stores. A list that is not strictly increasing is not a path and is refused
+// (DDT_ST_RANGE, sequence untouched).
 //
 // A CTA serves up to eight sequences (one per warp; one per CTA when the
 // batch is small, so every thread helps with one sequence's rows). A warp
-// walks its tree: every lane holds four tree slots in registers, one ballot
+// walks its tree: every lane holds NSL tree slots in registers, one ballot
 // per 32 slots finds the lowest-slot child whose token matches the target
-// argmax. Then all threads of the CTA move the accepted rows of all its
-// sequences in 16-byte chunks: every row into shared memory, a barrier, every
-// row out.
+// argmax. The warp then checks its path and lists the rows that move (byte
+// offsets of source and destination); all threads of the CTA copy the listed
+// rows of all its sequences as one flat range of 16-byte chunks, several
+// loads in flight per thread.
 #include "ddt_internal.cuh"
 
 namespace ddt {
@@ -27,16 +35,22 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kSlotsPerLane = kMaxQ / 32;
+constexpr int kBatch = 6;  // chunks a thread loads before storing any
 
 // seqs: sequences per CTA (1..kWarps); sequence blockIdx.x * seqs + w is
-// walked by warp w. The dynamic shared memory holds seqs x D rows.
-__global__ void __launch_bounds__(kThreads) k_accept_compact(AcceptCompactArgs a, int seqs) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+// walked by warp w. NSL = ceil(Q / 32) tree slots per lane. kCompact: the
+// compaction part is compiled in (a.do_compact); without it the kernel is
+// small enough for eight CTAs per SM.
+template <int NSL, bool kCompact>
+__global__ void __launch_bounds__(kThreads, kCompact ? 4 : 8)
+    k_accept_compact(AcceptCompactArgs a, int seqs) {
   __shared__ int32_t s_path[kWarps][kMaxQ + 1];
+  __shared__ long long s_src[kWarps][kMaxQ];  // byte offsets of the moved rows' sources
+  __shared__ long long s_dst[kWarps][kMaxQ];  // and destinations
   __shared__ int32_t s_len[kWarps];
   __shared__ int32_t s_status[kWarps];
-  __shared__ int32_t s_ok[kWarps];
+  __shared__ int32_t s_moves[kWarps];  // rows that move (0 for a refused sequence)
+  __shared__ int32_t s_hazard;
 
   // a kernel launched as this one's programmatic dependent (the split-KV
   // merge of the same step) needs nothing from it: let it start now
@@ -47,36 +61,48 @@ __global__ void __launch_bounds__(kThreads) k_accept_compact(AcceptCompactArgs a
   const int D = a.D;
   const int Q = a.Q;
   const long long b0 = (long long)blockIdx.x * seqs;
+  if (tid == 0) s_hazard = 0;
 
   if (warp < seqs) {
     const long long b = b0 + warp;
     if (b >= a.B) {
       if (lane == 0) s_len[warp] = -1;
     } else if (a.do_accept) {
-      int32_t tok[kSlotsPerLane], par[kSlotsPerLane], tgt[kSlotsPerLane];
+      int32_t tok[NSL], par[NSL], tgt[NSL];
 #pragma unroll
-      for (int k = 0; k < kSlotsPerLane; ++k) {
+      for (int k = 0; k < NSL; ++k) {
         const int c = lane + 32 * k;
         tok[k] = c < Q ? a.tokens[b * Q + c] : 0;
         par[k] = c < Q ? a.parents[b * Q + c] : -2;
         tgt[k] = c < Q ? a.target[b * Q + c] : 0;
       }
-      // target argmax at slot c, from the lane that holds it
-      auto target_at = [&](int c) -> int32_t {
-        int32_t v = tgt[0];
+      // value of a per-slot register array at slot c (the same c in every
+      // lane), from the lane holding it
+      auto at_slot = [&](const int32_t(&v)[NSL], int c) -> int32_t {
+        int32_t x = v[0];
 #pragma unroll
-        for (int k = 1; k < kSlotsPerLane; ++k)
-          if ((c >> 5) == k) v = tgt[k];
-        return __shfl_sync(0xffffffffu, v, c & 31);
+        for (int k = 1; k < NSL; ++k)
+          if ((c >> 5) == k) x = v[k];
+        return __shfl_sync(0xffffffffu, x, c & 31);
+      };
+      // the same with a slot of each lane's own
+      auto at_lane_slot = [&](const int32_t(&v)[NSL], int c) -> int32_t {
+        int32_t x = 0;
+#pragma unroll
+        for (int k = 0; k < NSL; ++k) {
+          const int32_t y = __shfl_sync(0xffffffffu, v[k], c & 31);
+          if ((c >> 5) == k) x = y;
+        }
+        return x;
       };
       unsigned long long visited_lo = 1ull, visited_hi = 0ull;  // slot 0 (root) is on the path
       int cur = 0, len = 0, st = 0;
       if (lane == 0) s_path[warp][0] = 0;
       for (int hop = 0; hop < D; ++hop) {
-        const int32_t want = target_at(cur);
+        const int32_t want = at_slot(tgt, cur);
         int nxt = -1;
 #pragma unroll
-        for (int k = 0; k < kSlotsPerLane; ++k) {
+        for (int k = 0; k < NSL; ++k) {
           const unsigned m = __ballot_sync(0xffffffffu, par[k] == cur && tok[k] == want);
           if (nxt < 0 && m) nxt = 32 * k + __ffs(m) - 1;
         }
@@ -92,17 +118,18 @@ __global__ void __launch_bounds__(kThreads) k_accept_compact(AcceptCompactArgs a
         if (lane == 0) s_path[warp][len] = nxt;
         cur = nxt;
       }
-      const int32_t bonus = target_at(cur);
+      const int32_t bonus = at_slot(tgt, cur);
       __syncwarp();
       int32_t* idx_o = a.accept_idx + b * (D + 1);
       int32_t* tok_o = a.out_tokens + b * (D + 1);
-      for (int d = lane; d <= D; d += 32) {
-        const int slot = d <= len ? s_path[warp][d] : -1;
-        idx_o[d] = slot;
-        int32_t t = -1;
-        if (d < len) t = a.tokens[b * Q + s_path[warp][d + 1]];
-        else if (d == len) t = bonus;
-        tok_o[d] = t;
+      for (int d0 = 0; d0 <= D; d0 += 32) {  // every lane takes part in the shuffles
+        const int d = d0 + lane;
+        const int nxt_slot = d < len ? s_path[warp][d + 1] : 0;
+        const int32_t t = at_lane_slot(tok, nxt_slot);  // token of the path's next node
+        if (d <= D) {
+          idx_o[d] = d <= len ? s_path[warp][d] : -1;
+          tok_o[d] = d < len ? t : (d == len ? bonus : -1);
+        }
       }
       if (lane == 0) {
         a.accept_len[b] = len;
@@ -115,135 +142,146 @@ __global__ void __launch_bounds__(kThreads) k_accept_compact(AcceptCompactArgs a
       if (lane == 0) {
         s_len[warp] = len;
         s_status[warp] = 0;
+        s_path[warp][0] = 0;  // the root; accept_idx[0] is not read
       }
-      for (int d = lane; d <= D && d <= len && len >= 0; d += 32)
+      for (int d = 1 + lane; d <= D && d <= len; d += 32)
         s_path[warp][d] = a.accept_idx[b * (D + 1) + d];
     }
   }
   __syncthreads();
 
-  if (!a.do_compact) {
+  if constexpr (!kCompact) {
     if (warp < seqs && lane == 0 && b0 + warp < a.B) a.status[b0 + warp] |= s_status[warp];
     return;
   }
-  // validity of every path (warp w decides for its sequence)
+  // each warp checks its sequence's path and lists the rows that move
   if (warp < seqs) {
     const long long b = b0 + warp;
     const int len = s_len[warp];
-    bool bad = true;
+    int moves = 0;
     if (b < a.B) {
       const int64_t L = a.prefix_len[b];
       const int64_t cap = (int64_t)a.max_pages * a.page_size;
       const int32_t* bt = a.block_table + b * a.max_pages;
-      bad = len < 0 || len > D || L < 0 || L + len >= cap;
+      bool bad = len < 0 || len > D || L < 0 || L + len >= cap;
+      bool hazard = false;
       if (!bad) {
+        // a path: 0 = s_0 < s_1 < ... < s_len, every slot inside the cache
         for (int d = 1 + lane; d <= len; d += 32) {
           const int64_t i = s_path[warp][d];
-          if (i < 0 || L + i >= cap) bad = true;
+          if (i <= s_path[warp][d - 1] || L + i >= cap) bad = true;
         }
         bad = __any_sync(0xffffffffu, bad);
       }
       if (!bad) {
-        for (int d = lane; d < 2 * len; d += 32) {
-          const int64_t slot = d < len ? L + s_path[warp][d + 1] : L + (d - len) + 1;
-          const int64_t row = slot_row(bt, a.page_size, slot);
-          if (row < 0 || row >= a.kv_rows) bad = true;
+        // rows of every source and destination slot inside the cache; the
+        // moved ones listed in order of d
+        for (int d0 = 1; d0 <= len; d0 += 32) {
+          const int d = d0 + lane;
+          bool mv = false;
+          int64_t src = 0, dst = 0;
+          if (d <= len) {
+            const int64_t s = s_path[warp][d];
+            src = slot_row(bt, a.page_size, L + s);
+            dst = slot_row(bt, a.page_size, L + d);
+            if (src < 0 || src >= a.kv_rows || dst < 0 || dst >= a.kv_rows) bad = true;
+            mv = s != d;
+            hazard |= mv && s <= len;  // a source that is also a destination
+          }
+          const unsigned m = __ballot_sync(0xffffffffu, mv);
+          if (mv) {
+            const int at = moves + __popc(m & ((1u << lane) - 1u));
+            s_src[warp][at] = src * a.row_bytes;
+            s_dst[warp][at] = dst * a.row_bytes;
+          }
+          moves += __popc(m);
         }
         bad = __any_sync(0xffffffffu, bad);
+        hazard = __any_sync(0xffffffffu, hazard);
       }
       if (lane == 0) {
         if (bad) {
           a.new_len[b] = (int32_t)L;
           a.status[b] |= s_status[warp] | DDT_ST_RANGE;
+        } else {
+          a.new_len[b] = (int32_t)(L + 1 + len);
+          a.status[b] |= s_status[warp];
+          if (hazard) s_hazard = 1;
         }
-        s_ok[warp] = !bad;
+        s_moves[warp] = bad ? 0 : moves;
       }
     } else if (lane == 0) {
-      s_ok[warp] = 0;
+      s_moves[warp] = 0;
     }
   }
   __syncthreads();
-  // every accepted row of the CTA's sequences into shared memory, then out:
-  // one flat range of 16-byte chunks over all of them, so every thread keeps
-  // several loads in flight whatever the sequences' lengths
-  const int chunks_per_row = a.row_bytes / 16;
-  int off[kWarps + 1];  // first chunk of each sequence in the flat range
+  // the listed rows of all the CTA's sequences as one flat range of 16-byte
+  // chunks (sequence, then d, then chunk), in batches of kBatch chunks per
+  // thread; consecutive batches follow increasing d within every sequence
+  const int cpr = a.row_bytes >> 4;  // chunks per row
+  int off[kWarps + 1];              // first flat row of each sequence
   off[0] = 0;
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w)
-    off[w + 1] = off[w] + ((w < seqs && s_ok[w]) ? s_len[w] * chunks_per_row : 0);
-  const int total = off[kWarps];
-  uint4* buf = reinterpret_cast<uint4*>(smem_raw);
-  auto locate = [&](int e, int& w, int& d, int& ch) {
-    w = 0;
-#pragma unroll
-    for (int k = 1; k < kWarps; ++k)
-      if (e >= off[k]) w = k;
-    const int r = e - off[w];
-    d = r / chunks_per_row + 1;
-    ch = r % chunks_per_row;
-  };
-  constexpr int kBatch = 4;  // loads a thread issues before storing any
-  for (int e0 = tid; e0 < total; e0 += kThreads * kBatch) {
+  for (int w = 0; w < kWarps; ++w) off[w + 1] = off[w] + (w < seqs ? s_moves[w] : 0);
+  const long long total = (long long)off[kWarps] * cpr;
+  const bool hazard = s_hazard != 0;
+  // chunk e = tid + kThreads * j; its (flat row, chunk) advanced without division
+  const int step_r = kThreads / cpr, step_c = kThreads % cpr;
+  int r = tid / cpr, c = tid % cpr;
+  for (long long e0 = 0; e0 < total; e0 += (long long)kThreads * kBatch) {
     uint4 v[kBatch];
-    size_t at[kBatch];
+    long long to[kBatch];
 #pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      const int e = e0 + k * kThreads;
-      if (e >= total) break;
-      int w, d, ch;
-      locate(e, w, d, ch);
-      const long long b = b0 + w;
-      const int64_t row = slot_row(a.block_table + b * a.max_pages, a.page_size,
-                                   (int64_t)a.prefix_len[b] + s_path[w][d]);
-      v[k] = reinterpret_cast<const uint4*>(a.kv + row * a.row_bytes)[ch];
-      at[k] = (size_t)w * D * chunks_per_row + (size_t)(d - 1) * chunks_per_row + ch;
+    for (int j = 0; j < kBatch; ++j) {
+      to[j] = -1;
+      if (e0 + tid + (long long)kThreads * j < total) {
+        int w = 0, first = 0;  // the sequence of flat row r and its first flat row
+#pragma unroll
+        for (int k = 1; k < kWarps; ++k)
+          if (r >= off[k]) {
+            w = k;
+            first = off[k];
+          }
+        const int i = r - first;
+        v[j] = *reinterpret_cast<const uint4*>(a.kv + s_src[w][i] + 16 * c);
+        to[j] = s_dst[w][i] + 16 * c;
+      }
+      c += step_c;
+      r += step_r;
+      if (c >= cpr) {
+        c -= cpr;
+        ++r;
+      }
     }
+    if (hazard) __syncthreads();  // every source of this batch read before any write
 #pragma unroll
-    for (int k = 0; k < kBatch; ++k)
-      if (e0 + k * kThreads < total) buf[at[k]] = v[k];
+    for (int j = 0; j < kBatch; ++j)
+      if (to[j] >= 0) *reinterpret_cast<uint4*>(a.kv + to[j]) = v[j];
   }
-  __syncthreads();
-  for (int e = tid; e < total; e += kThreads) {
-    int w, d, ch;
-    locate(e, w, d, ch);
-    const long long b = b0 + w;
-    const int64_t row = slot_row(a.block_table + b * a.max_pages, a.page_size,
-                                 (int64_t)a.prefix_len[b] + d);
-    reinterpret_cast<uint4*>(a.kv + row * a.row_bytes)[ch] =
-        buf[(size_t)w * D * chunks_per_row + (size_t)(d - 1) * chunks_per_row + ch];
-  }
-  if (tid < seqs && s_ok[tid]) {
-    const long long b = b0 + tid;
-    a.new_len[b] = (int32_t)(a.prefix_len[b] + 1 + s_len[tid]);
-    a.status[b] |= s_status[tid];
-  }
+}
+
+template <int NSL>
+void launch_k(const AcceptCompactArgs& a, int seqs, cudaStream_t stream) {
+  const long long grid = (a.B + seqs - 1) / seqs;
+  if (a.do_compact)
+    k_accept_compact<NSL, true><<<(unsigned)grid, kThreads, 0, stream>>>(a, seqs);
+  else
+    k_accept_compact<NSL, false><<<(unsigned)grid, kThreads, 0, stream>>>(a, seqs);
 }
 
 }  // namespace
 
-size_t accept_compact_smem_bytes(int32_t D, int32_t row_bytes) {
-  return (size_t)D * (size_t)row_bytes;
-}
-
 cudaError_t launch_accept_compact(const AcceptCompactArgs& a, cudaStream_t stream) {
   // sequences per CTA: one while the batch leaves SMs free (every thread then
-  // helps with that sequence's rows), up to eight (one per warp) beyond, as
-  // many as the rows' shared memory allows
-  const size_t per_seq = a.do_compact ? accept_compact_smem_bytes(a.D, a.row_bytes) : 0;
-  int seqs = 1;
-  if (a.B > 2LL * device_sm_count()) {
-    seqs = kWarps;
-    while (seqs > 1 && per_seq * (size_t)seqs > 200 * 1024) seqs /= 2;
+  // helps with that sequence's rows), eight (one per warp) beyond
+  const int seqs = a.B > 2LL * device_sm_count() ? kWarps : 1;
+  const int nsl = a.do_accept ? (a.Q + 31) / 32 : 1;
+  switch (nsl) {
+    case 1: launch_k<1>(a, seqs, stream); break;
+    case 2: launch_k<2>(a, seqs, stream); break;
+    case 3: launch_k<3>(a, seqs, stream); break;
+    default: launch_k<4>(a, seqs, stream); break;
   }
-  const size_t smem = per_seq * (size_t)seqs;
-  static int smem_set[64] = {};
-  if (smem + sizeof(int32_t) * kWarps * (kMaxQ + 4) > 48 * 1024) {  // with the static arrays
-    cudaError_t e = ensure_smem_limit(k_accept_compact, (int)smem, smem_set);
-    if (e != cudaSuccess) return e;
-  }
-  const long long grid = (a.B + seqs - 1) / seqs;
-  k_accept_compact<<<(unsigned)grid, kThreads, smem, stream>>>(a, seqs);
   return cudaGetLastError();
 }
 

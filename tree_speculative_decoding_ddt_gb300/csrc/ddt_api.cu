@@ -50,7 +50,7 @@ int check_compact(int32_t B, int32_t D, int32_t row_bytes, int32_t page_size, in
   if (B < 1 || D < 0 || row_bytes < 1 || page_size < 1 || max_pages < 1 || kv_rows < 0)
     return DDT_EINVAL;
   if (row_bytes % 16 != 0 || !aligned16(kv)) return DDT_EUNSUPPORTED;
-  if ((int64_t)D * row_bytes > 196608) return DDT_EUNSUPPORTED;
+  if (D > DDT_MAX_Q - 1) return DDT_EUNSUPPORTED;  // a path of a tree of at most DDT_MAX_Q slots
   return DDT_OK;
 }
 

@@ -43,7 +43,6 @@ struct AcceptCompactArgs {
   int32_t* status;
 };
 cudaError_t launch_accept_compact(const AcceptCompactArgs& a, cudaStream_t stream);
-size_t accept_compact_smem_bytes(int32_t D, int32_t row_bytes);
 
 // B. verify attention, fp32 SIMT path (no workspace).
 cudaError_t launch_verify_attn_f32(const ddt_attn_dims& d, const float* q_lat, const float* q_pe,

@@ -427,3 +427,36 @@ def loop_drafter_table(cid: int, golden: np.ndarray, V: int, hit, dtype: str,
                 rows[j, golden[b, j]] = (round_bf16(top) if dtype == "bf16" else top)[0]
         out[b] = rows
     return out
+
+
+# ------------------------------------------------------------ stress point
+
+def stress_inputs(B: int, D: int, K: int, V: int, device, seed: int = 99):
+    """Drafter and target of the build / accept / compaction stress point (B
+    sequences, D depths, K >= 2 candidates, budget 2 * D), drawn with torch on
+    ``device``: at depth 1 the two best candidates score -0.01 and -0.02, at
+    every deeper level the best scores -0.001, all others -30 or less; the K
+    candidate tokens of a depth are distinct. The tree's first D pops are then
+    the rank-0 chain (slots 1..D, all above -0.02), then the rank-1 child of
+    the root (slot D+1) and its rank-0 chain (slots D+2 .. 2D). The target
+    picks that rank-1 child at the root and the rank-0 candidate below it, so
+    every sequence accepts the D nodes of slots D+1 .. 2D and compaction
+    moves D rows (slot D+d to slot d), none of them in place.
+    Returns (topk_logp f32 [B,D,K], topk_ids i32 [B,D,K], root_tok i32 [B],
+    target_argmax i32 [B, 2D+1])."""
+    import torch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    Q = 2 * D + 1
+    logp = -torch.rand((B, D, K), generator=gen, device=device) * 4.0 - 30.0
+    logp[:, 0, 0] = -0.01
+    logp[:, 0, 1] = -0.02
+    logp[:, 1:, 0] = -0.001
+    logp = logp.sort(dim=-1, descending=True).values.contiguous()
+    base = torch.randint(0, V, (B, D, 1), generator=gen, device=device, dtype=torch.int64)
+    ids = ((base + torch.arange(K, device=device)) % V).to(torch.int32).contiguous()
+    root = torch.randint(0, V, (B,), generator=gen, device=device, dtype=torch.int32)
+    target = torch.zeros((B, Q), dtype=torch.int32, device=device)
+    target[:, 0] = ids[:, 0, 1]
+    target[:, D + 1: 2 * D] = ids[:, 1:, 0]  # slot D+1+k (depth 1+k) -> its rank-0 child
+    return logp, ids, root, target
