@@ -38,6 +38,19 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
                : "memory");
 }
+// The same without release semantics. A release at cluster scope makes the
+// arriving thread wait until the memory operations it has issued or observed
+// are visible across the cluster, which on GB300 costs about a microsecond
+// while the SM has bulk copies and tensor loads in flight. Relays use this
+// form when the arrive only passes on an event that has already completed
+// where the data lives (a tile landed in this CTA's shared memory, an S buffer
+// read into registers, a copy out of a slot finished): the waiter acts on
+// this CTA's memory only after the arrive, which is issued only after that
+// completion was observed here.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
+               : "memory");
+}
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -273,6 +286,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
       "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
       : DDT_R8(0), DDT_R8(8), DDT_R8(16), DDT_R8(24)
+      : "r"(taddr)
+      : "memory");
+}
+// 128 consecutive 32-bit columns of this thread's TMEM lane in one request.
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x128.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, %96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%128];"
+      : DDT_R8(0), DDT_R8(8), DDT_R8(16), DDT_R8(24), DDT_R8(32), DDT_R8(40), DDT_R8(48),
+        DDT_R8(56), DDT_R8(64), DDT_R8(72), DDT_R8(80), DDT_R8(88), DDT_R8(96), DDT_R8(104),
+        DDT_R8(112), DDT_R8(120)
       : "r"(taddr)
       : "memory");
 }

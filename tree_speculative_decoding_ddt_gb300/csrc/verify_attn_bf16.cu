@@ -796,7 +796,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (tid == 64) {
           if (jj + kMsgSlots < nt) mbar_expect_tx(bar(B_P_FULL + mb), kMsgBytes);
-          mbar_arrive_cluster(pfree_peer0 + 8 * mb);
+          mbar_arrive_cluster_relaxed(pfree_peer0 + 8 * mb);
         }
       }
       // ---- epilogue: O / l ---------------------------------------------------

@@ -35,10 +35,12 @@
 // S tile is as wide as TMEM allows (N = 128) to keep the MMA count per key low.
 //
 // Warp roles (352 threads). S-CTAs: warp 0 TMA (its Q rows, then its key
-// halves), warp 1 TMEM allocation and (rank 0) the first MMA issuer, warps
-// 2-9 softmax (warp w: lane quadrant w % 4, key half (w - 2) / 4), warp 10
-// (rank 0) the second MMA issuer (the two take alternate key tiles, which
-// keeps the tensor pipe busy while one of them is issuing). O-CTAs: warp 0
+// halves), warp 1 TMEM allocation and then (rank 0) the first MMA issuer or
+// (rank 1) the relay that tells rank 0 an S buffer has been read, warps 2-9
+// softmax (two groups of four warps taking alternate key tiles; warp w holds
+// lane quadrant w % 4), warp 10 (rank 0) the second MMA issuer (the two take
+// alternate key tiles, which keeps the tensor pipe busy while one of them is
+// issuing) or (rank 1) the relay of its key halves' arrival. O-CTAs: warp 0
 // TMA, warp 1 TMEM allocation and (rank 2) the PV issuer, warps 2-5 row warps
 // (rescales, output), warp 6 of rank 2 the fused tree build.
 #include <cuda_bf16.h>
@@ -95,6 +97,7 @@ constexpr uint32_t O_RING = 0;
 constexpr uint32_t O_MSG = O_RING + kStagesV * kTileV;
 constexpr uint32_t O_FIN = O_MSG + kMsgSlots * kMsgStride;
 constexpr uint32_t O_GO = O_FIN + 512;  // message index of the current GO call (-1: the end)
+constexpr uint32_t O_PEERFLAG = O_FIN + 768;  // rank 2: rank 3's rescale flags [slot][16 B]
 constexpr uint32_t O_BUILD = O_FIN + 1024;
 constexpr uint32_t kBuildBytes = (uint32_t)tb::smem_bytes(kFuseMaxCand, 1);
 constexpr uint32_t O_END = O_BUILD + ((kBuildBytes + 1023) & ~1023u);
@@ -117,8 +120,9 @@ enum Bar {
   B_RING_PEER = B_RING_FULL + kStagesK,   // +stage; rank 0: rank 1's key half landed (relay)
   B_RING_EMPTY = B_RING_PEER + kStagesK,  // +stage; both (pair MMA commit)
   B_S_FULL = B_RING_EMPTY + kStagesK,     // +buffer; both (pair MMA commit)
-  B_S_EMPTY = B_S_FULL + 2,               // +buffer; rank 0: the 8 warps of one group
-  B_Q_FULL = B_S_EMPTY + 2,               // this CTA's Q rows landed
+  B_S_EMPTY = B_S_FULL + 2,               // +buffer; rank 0: its 4 warps of one group + rank 1's relay
+  B_S_READ = B_S_EMPTY + 2,               // +buffer; rank 1: its 4 warps of one group read S
+  B_Q_FULL = B_S_READ + 2,                // this CTA's Q rows landed
   B_Q_TMEM = B_Q_FULL + 1,                // rank 0: 16 warps, rank 1: 8
   B_P_FREE = B_Q_TMEM + 1,                // +O-CTA slot; both (PV commit from rank 2)
   B_STAGE_FREE = B_P_FREE + kMsgSlots,    // +staging slot; the O-CTA saw the copy land
@@ -128,7 +132,7 @@ enum Bar {
   B_HALF_PEER = B_HALF_FULL + kStagesV,   // +stage; rank 2: rank 3's value half landed (relay)
   B_HALF_EMPTY = B_HALF_PEER + kStagesV,  // +stage; both (PV commit)
   B_P_FULL = B_HALF_EMPTY + kStagesV,     // +slot; completed by the S-CTA's copy
-  B_P_PEER = B_P_FULL + kMsgSlots,        // +slot; rank 2: rank 3's message landed (relay)
+  B_P_PEER = B_P_FULL + kMsgSlots,        // +slot; rank 2: rank 3's message landed (its flags, 16 B)
   B_PV_DONE = B_P_PEER + kMsgSlots,       // +slot; both (PV commit)
   B_GO = B_PV_DONE + kMsgSlots,           // both: the PV issuer calls the row warps (a rescale, or the end)
   B_O_READY = B_GO + 1,                   // rank 2: +0 its row warps, +1 rank 3's, rescale done
@@ -371,7 +375,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       }
       for (int s = 0; s < 2; ++s) {
         mbar_init(bar(B_S_FULL + s), 1);
-        mbar_init(bar(B_S_EMPTY + s), 8);
+        mbar_init(bar(B_S_EMPTY + s), 5);
+        mbar_init(bar(B_S_READ + s), 4);
       }
       for (int s = 0; s < kMsgSlots; ++s) mbar_init(bar(B_P_FREE + s), 1);
       for (int s = 0; s < kStageSlots; ++s) mbar_init(bar(B_STAGE_FREE + s), 1);
@@ -398,8 +403,10 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_FIN_FULL), 1);
       mbar_init(bar(B_TAIL_OK), 2);
       mbar_init(bar(B_MMA_DONE), 1);
-      for (int s = 0; s < kMsgSlots && s < n_msgs; ++s)
+      for (int s = 0; s < kMsgSlots && s < n_msgs; ++s) {
         mbar_expect_tx(bar(B_P_FULL + s), kMsgBytes);
+        if (rank == 2) mbar_expect_tx(bar(B_P_PEER + s), 16);  // rank 3's flags
+      }
       mbar_expect_tx(bar(B_FIN_FULL), kFinBytes);
     }
     fence_mbar_init();
@@ -509,7 +516,21 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
             failed = true;
             break;
           }
-          mbar_arrive_cluster(peer0 + 8 * (u % kStagesK));
+          mbar_arrive_cluster_relaxed(peer0 + 8 * (u % kStagesK));
+        }
+      }
+    } else if (rank == 1 && warp == 1) {
+      // relay: this CTA's group has read S buffer jj & 1 -> rank 0's MMA
+      // issuers (the softmax warps arrive locally; a release at cluster scope
+      // from each of them held them up for about a microsecond per tile)
+      if (lane == 0) {
+        const uint32_t s_empty0 = map_peer(bar(B_S_EMPTY), 0);
+        for (int jj = 0; jj < nt; ++jj) {
+          if (!mbar_wait(bar(B_S_READ + (jj & 1)), (jj >> 1) & 1)) {
+            failed = true;
+            break;
+          }
+          mbar_arrive_cluster_relaxed(s_empty0 + 8 * (jj & 1));
         }
       }
     } else if (warp >= 2 && warp <= 9) {
@@ -571,7 +592,6 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       if (!bar1_and(q_ok, 256)) failed = true;
       const uint32_t msg_peer0 = map_peer(sbase + O_MSG, rank + 2);
       const uint32_t pfull_peer0 = map_peer(bar(B_P_FULL), rank + 2);
-      const uint32_t s_empty0 = map_peer(bar(B_S_EMPTY), 0);
       const uint32_t bar_in = 2 + 2 * qd + g;         // handoff to this group
       const uint32_t bar_out = 2 + 2 * qd + (g ^ 1);  // handoff to the other group
       const uint32_t bar_grp = 10 + g;                // the group's four warps
@@ -590,20 +610,14 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         if (ok) {
           ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar(B_S_FULL + g), (jj >> 1) & 1));
           tc_fence_after();
-          uint32_t sa[32];
+          uint32_t sa[128];  // the whole S row in one request, so the buffer is freed soon
+          tmem_ld128(t_lane + kTmemS + g * kBS, sa);
+          tmem_ld_wait();
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            tmem_ld32(t_lane + kTmemS + g * kBS + 32 * q, sa);
-            tmem_ld_wait();
-#pragma unroll
-            for (int k = 0; k < 32; ++k) x[32 * q + k] = __uint_as_float(sa[k]);
-          }
+          for (int k = 0; k < 128; ++k) x[k] = __uint_as_float(sa[k]);
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) {
-            if (rank == 0) mbar_arrive(bar(B_S_EMPTY + g));
-            else mbar_arrive_cluster(s_empty0 + 8 * g);
-          }
+          if (lane == 0) mbar_arrive(bar((rank == 0 ? B_S_EMPTY : B_S_READ) + g));
 #pragma unroll
           for (int kb = 0; kb < 2; ++kb) {
             const int blk = 2 * tile + kb;
@@ -820,7 +834,6 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         // Before PV of message jj the O rows of a quadrant whose flag is set in
         // the message are multiplied by the row's factor; this thread reads the
         // flags of both CTAs' messages and calls the row warps only then.
-        const uint32_t msg3 = map_peer(sbase + O_MSG, 3);
         const uint32_t go3 = map_peer(bar(B_GO), 3);
         const uint32_t goidx3 = map_peer(sbase + O_GO, 3);
         uint32_t n_go2 = 0, n_go3 = 0;  // completed rescale calls per CTA
@@ -832,10 +845,12 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
             failed = true;
             break;
           }
+          // rank 3's flags of message jj + kMsgSlots complete the next phase
+          if (jj + kMsgSlots < n_msgs) mbar_expect_tx(bar(B_P_PEER + mb), 16);
           if (jj > 0) {
             const uint4 f2 =
                 *reinterpret_cast<const uint4*>(smem + O_MSG + mb * kMsgStride + kPBytes + kHM * 4);
-            const uint4 f3 = ld_cluster_v4(msg3 + mb * kMsgStride + kPBytes + kHM * 4);
+            const uint4 f3 = *reinterpret_cast<const uint4*>(smem + O_PEERFLAG + 16 * mb);
             const bool r2 = (f2.x | f2.y | f2.z | f2.w) != 0;
             const bool r3 = (f3.x | f3.y | f3.z | f3.w) != 0;
             if (r2 || r3) {
@@ -899,7 +914,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
             failed = true;
             break;
           }
-          mbar_arrive_cluster(peer2 + 8 * (u % kStagesV));
+          mbar_arrive_cluster_relaxed(peer2 + 8 * (u % kStagesV));
         }
       }
     } else if (warp == 7) {
@@ -917,8 +932,16 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
             break;
           }
           if (jj + kMsgSlots < n_msgs) mbar_expect_tx(bar(B_P_FULL + mb), kMsgBytes);
-          mbar_arrive_cluster(stage_free0 + 8 * (jj % kStageSlots));
-          if (rank == 3) mbar_arrive_cluster(ppeer2 + 8 * mb);
+          mbar_arrive_cluster_relaxed(stage_free0 + 8 * (jj % kStageSlots));
+          if (rank == 3) {
+            // the relay to rank 2's PV issuer carries the message's rescale
+            // flags: one 16-byte asynchronous store that completes rank 2's
+            // P_PEER phase on arrival (so the issuer reads them locally)
+            const uint4 fl =
+                *reinterpret_cast<const uint4*>(smem + O_MSG + mb * kMsgStride + kPBytes + kHM * 4);
+            st_async_v4(map_peer(sbase + O_PEERFLAG, 2) + 16 * mb, fl.x, fl.y, fl.z, fl.w,
+                        ppeer2 + 8 * mb);
+          }
         }
       }
     } else if (warp >= 2 && warp <= 5) {
