@@ -63,20 +63,34 @@ def test_noalloc_matches_the_workspace_entry_point_on_two_calls(cfg, mods, attn_
 
 
 def test_noalloc_refuses_a_request_larger_than_its_scratch():
-    # the deep long-context step splits its key range into more partials than
-    # the fixed scratch holds: refused on the host, nothing enqueued
-    w = WL.CONFIGS["c4"]
-    dims = DB.attn_dims(w.B, w.Q, w.H, w.C, w.R, 64, 1, 8 * 33024, DB.DDT_BF16, w.scale, 32833)
-    need = DB.ddt_verify_attn_workspace_size(dims)
-    assert need > (32 << 20)
-    small = WL.CONFIGS["c2"].with_(B=1, prefix=64, V=4096)
-    _, args, lay = _inputs(small)
-    lib = DB.load()
+    # Dims over a wide grid: any whose split-KV scratch would exceed the fixed
+    # array are refused on the host before anything is enqueued (the buffers
+    # passed are far too small for those dims, which is safe only because
+    # nothing is launched). The plans keep the number of key ranges near one
+    # wave of clusters, so the scratch they need may stay below the array for
+    # every dims of the grid; the largest need found is then checked to fit.
     import ctypes
-    out = torch.empty((w.B, w.Q, w.H, w.C), dtype=torch.bfloat16, device="cuda")
-    st = torch.zeros((w.B,), dtype=torch.int32, device="cuda")
-    rc = lib.ddt_verify_attn_noalloc(ctypes.byref(dims), args[0].data_ptr(), args[1].data_ptr(),
-                                     args[2].data_ptr(), args[3].data_ptr(), args[4].data_ptr(),
-                                     args[5].data_ptr(), out.data_ptr(), None, st.data_ptr(),
-                                     torch.cuda.current_stream().cuda_stream)
-    assert rc == -4  # DDT_EWORKSPACE
+    small = WL.CONFIGS["c2"].with_(B=1, prefix=64, V=4096)
+    _, args, _ = _inputs(small)
+    lib = DB.load()
+    out = torch.empty((1, 1, 1, 512), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros((64,), dtype=torch.int32, device="cuda")
+    largest, refused = 0, 0
+    for B in (1, 2, 8, 64):
+        for Q in (1, 17, 65, 128):
+            for H in (16, 64, 128):
+                for L in (1 << 12, 1 << 17, 1 << 22):
+                    dims = DB.attn_dims(B, Q, H, 512, 64, 64, (L + Q + 63) // 64,
+                                        B * (L + Q + 64), DB.DDT_BF16, 0.07, L + Q)
+                    need = DB.ddt_verify_attn_workspace_size(dims)
+                    largest = max(largest, need)
+                    if need > (32 << 20):
+                        rc = lib.ddt_verify_attn_noalloc(
+                            ctypes.byref(dims), args[0].data_ptr(), args[1].data_ptr(),
+                            args[2].data_ptr(), args[3].data_ptr(), args[4].data_ptr(),
+                            args[5].data_ptr(), out.data_ptr(), None, st.data_ptr(),
+                            torch.cuda.current_stream().cuda_stream)
+                        assert rc == -4  # DDT_EWORKSPACE
+                        refused += 1
+    torch.cuda.synchronize()
+    assert refused > 0 or 0 < largest <= (32 << 20)

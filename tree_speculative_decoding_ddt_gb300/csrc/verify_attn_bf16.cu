@@ -966,8 +966,8 @@ struct KernelCost {
   double unit_start;  // cycles
   double per_64_keys; // cycles per 64 keys of one unit
 };
-constexpr KernelCost kCost128 = {128, 64, 25000.0, 2300.0};
-constexpr KernelCost kCost256 = {256, 128, 45000.0, 2085.0};
+constexpr KernelCost kCost128 = {128, 64, 45000.0, 2300.0};
+constexpr KernelCost kCost256 = {256, 128, 40000.0, 1840.0};
 constexpr double kMergeBytesPerCycle = 3200.0;  // about 6.6 TB/s at 2.07 GHz
 
 Plan make_plan(const ddt_attn_dims& d, const KernelCost& k, long long per_wave) {
@@ -984,7 +984,7 @@ Plan make_plan(const ddt_attn_dims& d, const KernelCost& k, long long per_wave) 
   pl.n_split = 1;
   for (long long s = 1; s <= 64 && s <= n_tiles; ++s) {
     const long long units = base * s;
-    const long long waves = (units + per_wave - 1) / per_wave;
+    const double waves = (double)((units + per_wave - 1) / per_wave);
     // tiles of the longest unit (the kernels give every unit but the last
     // one tile more than an even share when the range is split)
     const long long tpu = s > 1 ? (n_tiles + s) / s : n_tiles;
@@ -992,7 +992,7 @@ Plan make_plan(const ddt_attn_dims& d, const KernelCost& k, long long per_wave) 
                         (double)tpu * (double)(k.keys_per_tile / 64) * k.per_64_keys;
     const double merge =
         s > 1 ? 3000.0 + (double)(s + 1) * rows_total * 1028.0 / kMergeBytesPerCycle : 0.0;
-    const double cost = (double)waves * unit + merge;
+    const double cost = waves * unit + merge;
     if (cost < pl.cost - 1e-9) {
       pl.cost = cost;
       pl.n_split = (int)s;
@@ -1009,20 +1009,20 @@ Plan plan_256(const ddt_attn_dims& d) {
   return make_plan(d, kCost256, per_wave);
 }
 
-// The launch's plan. The 256-row kernel moves half the bytes per FLOP but
-// pads a sequence's Q*H rows to a multiple of 256: it is taken when that
-// padding is at most 1/12 of the rows (e.g. q_len 65 x 64 heads: 4160 rows
-// in 4352), else the 128-row kernel (q_len 17 x 64 heads: 1088 rows would
-// fill 1280). The environment variable DDT_VERIFY_ATTN_ROWS (128 or 256)
+// The launch's plan: the cheaper of the two kernels by the cost model. The
+// 256-row kernel moves half the bytes per FLOP and runs a key tile faster per
+// SM, but pads a sequence's Q*H rows to a multiple of 256 (q_len 65 x 64
+// heads: 4160 rows in 4352; q_len 17 x 64 heads: 1088 rows in 1280), which
+// the model counts as work. The environment variable DDT_VERIFY_ATTN_ROWS (128 or 256)
 // overrides the choice.
 Plan choose_plan(const ddt_attn_dims& d) {
   const char* env = getenv("DDT_VERIFY_ATTN_ROWS");
   if (env != nullptr && strcmp(env, "128") == 0) return plan_128(d);
   if (env != nullptr && strcmp(env, "256") == 0) return plan_256(d);
-  const long long QH = (long long)d.Q * d.H;
-  const long long pad = ((QH + 255) / 256) * 256 - QH;
-  const bool pair_ok = verify_attn_pair_clusters_per_wave() > 0;
-  return (pair_ok && QH >= 256 && pad * 12 <= QH) ? plan_256(d) : plan_128(d);
+  const Plan p128 = plan_128(d);
+  if (verify_attn_pair_clusters_per_wave() <= 0) return p128;
+  const Plan p256 = plan_256(d);
+  return p256.cost < p128.cost ? p256 : p128;
 }
 
 size_t workspace_of(const ddt_attn_dims& d, const Plan& pl) {
