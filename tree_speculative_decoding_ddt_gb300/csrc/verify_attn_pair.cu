@@ -80,7 +80,7 @@ constexpr uint32_t kPBytes = kHM * 128;                   // P: 128 rows x 64 ke
 constexpr uint32_t kMsgBytes = kPBytes + kHM * 4 + 16;    // P | per-row factor | 4 warp flags
 constexpr uint32_t kMsgStride = 17408;
 constexpr uint32_t kFinBytes = kHM * 4;
-constexpr uint32_t kQlBytes = kHM * kC * 2;               // q_lat rows: 128 KB
+constexpr uint32_t kQlHalf = kHM * (kC / 2) * 2;          // half the q_lat dims of the rows: 64 KB
 constexpr uint32_t kQpBytes = kHM * kR * 2;               // q_pe rows: 16 KB
 constexpr uint32_t kOutStride = 1040;
 
@@ -106,7 +106,7 @@ constexpr int kBtMax = 1024;
 constexpr uint32_t OFF_BT = (S_END > O_END ? S_END : O_END);
 constexpr uint32_t OFF_BAR = OFF_BT + kBtMax * 4;
 constexpr uint32_t kSmemBytes = OFF_BAR + 1024 + 1024;
-static_assert(kQlBytes <= kStagesK * kTileK, "q_lat is staged in the S-CTA ring");
+static_assert(kQlHalf <= kTileK, "each half of q_lat is staged in one stage of the key ring");
 static_assert(S_STAGE % 1024 == 0 && O_MSG % 1024 == 0 && kMsgStride % 1024 == 0, "alignment");
 static_assert(kMsgBytes <= kMsgStride && kMsgBytes % 16 == 0, "message size");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -122,8 +122,9 @@ enum Bar {
   B_S_FULL = B_RING_EMPTY + kStagesK,     // +buffer; both (pair MMA commit)
   B_S_EMPTY = B_S_FULL + 2,               // +buffer; rank 0: its 4 warps of one group + rank 1's relay
   B_S_READ = B_S_EMPTY + 2,               // +buffer; rank 1: its 4 warps of one group read S
-  B_Q_FULL = B_S_READ + 2,                // this CTA's Q rows landed
-  B_Q_TMEM = B_Q_FULL + 1,                // rank 0: 16 warps, rank 1: 8
+  B_Q_FULL = B_S_READ + 2,                // +half; q_lat dims [256h, 256h + 256) landed (h = 0: and q_pe)
+  B_Q_LOCAL = B_Q_FULL + 2,               // +half; this CTA's group h has moved its half to TMEM
+  B_Q_TMEM = B_Q_LOCAL + 2,               // rank 0: all q_lat of both CTAs in TMEM (8 + 8 warps)
   B_P_FREE = B_Q_TMEM + 1,                // +O-CTA slot; both (PV commit from rank 2)
   B_STAGE_FREE = B_P_FREE + kMsgSlots,    // +staging slot; the O-CTA saw the copy land
   B_TREE = B_STAGE_FREE + kStageSlots,    // ancestor words of the fused build
@@ -303,15 +304,19 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   const int32_t* bt = p.block_table + (size_t)b * p.max_pages;
   const long long row0 = (long long)b * QH + (long long)rt * kTM + half * kHM;  // this CTA's rows
 
-  // Q depends on no check: each S-CTA starts the load of its 128 rows first
-  // (q_lat into the key ring, which the keys take over once it is in TMEM;
-  // q_pe into its own area, where it stays as an MMA operand)
+  // Q depends on no check: each S-CTA starts the load of its 128 rows first.
+  // q_lat comes in two halves, one per stage of the key ring, so that each
+  // stage takes its first key tile as soon as its half has moved to TMEM;
+  // q_pe goes to its own area, where it stays as an MMA operand.
   if (s_side && tid == 0) {
-    mbar_init(bar(B_Q_FULL), 1);
+    mbar_init(bar(B_Q_FULL + 0), 1);
+    mbar_init(bar(B_Q_FULL + 1), 1);
     fence_mbar_init();
-    mbar_expect_tx(bar(B_Q_FULL), kQlBytes + kQpBytes);
-    tma_load_3d(sbase + S_RING, &tm_ql, 0, (int)row0, 0, bar(B_Q_FULL));
-    tma_load_2d(sbase + S_QPE, &tm_qp, 0, (int)row0, bar(B_Q_FULL));
+    mbar_expect_tx(bar(B_Q_FULL + 0), kQlHalf + kQpBytes);
+    tma_load_3d(sbase + S_RING, &tm_ql, 0, (int)row0, 0, bar(B_Q_FULL + 0));
+    tma_load_2d(sbase + S_QPE, &tm_qp, 0, (int)row0, bar(B_Q_FULL + 0));
+    mbar_expect_tx(bar(B_Q_FULL + 1), kQlHalf);
+    tma_load_3d(sbase + S_RING + kTileK, &tm_ql, 0, (int)row0, 4, bar(B_Q_FULL + 1));
   }
 
   // ---- capacity and page checks: identical decision in all four CTAs ------
@@ -348,7 +353,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   if (nt == 0) {
     // nothing may land after exit: a Q load still pending when the bounded
     // wait gives up is reported, as on the main path
-    if (s_side && tid == 0 && !mbar_wait(bar(B_Q_FULL), 0)) atomicOr(p.status + b, DDT_ST_TIMEOUT);
+    if (s_side && tid == 0 && (!mbar_wait(bar(B_Q_FULL + 0), 0) || !mbar_wait(bar(B_Q_FULL + 1), 0)))
+      atomicOr(p.status + b, DDT_ST_TIMEOUT);
     write_empty(p, b, rt, sp, rank);
     if (code && rt == 0 && sp == 0 && rank == 0 && tid == 0) atomicOr(p.status + b, code);
     if (designated && rank == 2 && warp == 6) {
@@ -380,7 +386,9 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       }
       for (int s = 0; s < kMsgSlots; ++s) mbar_init(bar(B_P_FREE + s), 1);
       for (int s = 0; s < kStageSlots; ++s) mbar_init(bar(B_STAGE_FREE + s), 1);
-      mbar_init(bar(B_Q_TMEM), rank == 0 ? 16 : 8);
+      mbar_init(bar(B_Q_LOCAL + 0), 4);
+      mbar_init(bar(B_Q_LOCAL + 1), 4);
+      mbar_init(bar(B_Q_TMEM), 16);  // used on rank 0
       mbar_init(bar(B_MMA_DONE), 2);
       if (builds) {
         mbar_init(bar(B_TREE), 1);
@@ -441,12 +449,12 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         prefetch_tmap(&tm_k);
         int u = 0;
-        if (!mbar_wait_cluster(bar(B_Q_TMEM), 0)) failed = true;  // q_lat has left the ring
-        if (!mbar_wait(bar(B_Q_FULL), 0)) failed = true;
         for (; u < nt && !failed; ++u) {  // this CTA's 64-key half of tile u, one request
           const int slot = u % kStagesK;
-          if (u >= kStagesK &&
-              !mbar_wait_cluster(bar(B_RING_EMPTY + slot), ((u / kStagesK) - 1) & 1)) {
+          // the stage is free once its half of q_lat has left it, then after the
+          // MMAs of the tile two back
+          if (u < kStagesK ? !mbar_wait(bar(B_Q_LOCAL + slot), 0)
+                           : !mbar_wait_cluster(bar(B_RING_EMPTY + slot), ((u / kStagesK) - 1) & 1)) {
             failed = true;
             break;
           }
@@ -561,17 +569,17 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         vis0 = vb[0];
         if (W > 1) vis1 = vb[1];
       }
-      // q_lat row r -> TMEM columns [0,256) (bf16 pairs); group 0 moves
-      // chunks 0-3, group 1 chunks 4-7
-      const bool q_ok = __all_sync(0xffffffffu, mbar_wait(bar(B_Q_FULL), 0));
+      // q_lat row r -> TMEM columns [0,256) (bf16 pairs); group g moves
+      // chunks 4g .. 4g + 3, which its half of the ring holds
+      const bool q_ok = __all_sync(0xffffffffu, mbar_wait(bar(B_Q_FULL + g), 0));
       if (q_ok) {
-        const unsigned char* qrow = smem + S_RING + r * 128;
+        const unsigned char* qrow = smem + S_RING + g * kTileK + r * 128;
 #pragma unroll 1
         for (int c = 4 * g; c < 4 * g + 4; ++c) {
           uint32_t v[32];
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            const uint4 x = *reinterpret_cast<const uint4*>(qrow + c * (kHM * 128) +
+            const uint4 x = *reinterpret_cast<const uint4*>(qrow + (c - 4 * g) * (kHM * 128) +
                                                              ((q ^ (r & 7)) << 4));
             v[4 * q + 0] = x.x;
             v[4 * q + 1] = x.y;
@@ -586,8 +594,11 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(bar(B_Q_TMEM));
-        if (rank == 1) mbar_arrive_cluster(map_peer(bar(B_Q_TMEM), 0));
+        mbar_arrive(bar(B_Q_LOCAL + g));  // this stage of the ring may take key tiles
+        // rank 0's MMA issuers need the q_lat of both CTAs in TMEM (the
+        // arrive passes on stores to TMEM that have completed here)
+        if (rank == 0) mbar_arrive(bar(B_Q_TMEM));
+        else mbar_arrive_cluster_relaxed(map_peer(bar(B_Q_TMEM), 0));
       }
       if (!bar1_and(q_ok, 256)) failed = true;
       const uint32_t msg_peer0 = map_peer(sbase + O_MSG, rank + 2);
@@ -1076,7 +1087,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 // Values: the c_kv part as {64 dims, rows, 4 chunks, 2 halves} (strides: row,
 // 128 B, 512 B); a box of {64, 64, 2, 2} at chunk 2h holds dims
 // [128h, 128h + 128) and [256 + 128h, 256 + 128h + 128) as four 8 KB chunks.
-// Queries: as in the 128-row kernel, 128 rows per box.
+// Queries: 128 rows per box; q_lat in two boxes of four 64-dim chunks each.
 bool encode_maps(CUtensorMap* mk, CUtensorMap* mv, CUtensorMap* ml, CUtensorMap* mp,
                  const void* kv, uint64_t kv_rows, const void* q_lat, const void* q_pe,
                  uint64_t q_rows) {
@@ -1105,7 +1116,7 @@ bool encode_maps(CUtensorMap* mk, CUtensorMap* mv, CUtensorMap* ml, CUtensorMap*
   {
     cuuint64_t dims[3] = {64, q_rows, (cuuint64_t)(kC / 64)};
     cuuint64_t str[2] = {(cuuint64_t)kC * 2, 128};
-    cuuint32_t box[3] = {64, (cuuint32_t)kHM, (cuuint32_t)(kC / 64)};
+    cuuint32_t box[3] = {64, (cuuint32_t)kHM, (cuuint32_t)(kC / 128)};  // half the chunks
     if (fn(ml, bf, 3, const_cast<void*>(q_lat), dims, str, box, e4, il, sw, l2, oob) !=
         CUDA_SUCCESS)
       return false;
