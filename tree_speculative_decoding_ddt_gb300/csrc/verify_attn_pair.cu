@@ -169,8 +169,12 @@ struct Params {
   __nv_bfloat16* part_o;
   float* part_lse;
   int fuse;
+  int longest_first;  // clusters take the sequences in order of decreasing prefix length
   TreeFuse tf;
 };
+
+// Sequences per launch up to which the clusters take them longest first.
+constexpr int kLongestFirstMax = 352;
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -298,7 +302,30 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   const long long unit = blockIdx.x >> 2;
   const int sp = (int)(unit % p.n_split);
   const int rt = (int)((unit / p.n_split) % p.n_rt);
-  const int b = (int)(unit / ((long long)p.n_split * p.n_rt));
+  int b = (int)(unit / ((long long)p.n_split * p.n_rt));
+  if (p.longest_first) {
+    // Clusters start roughly in launch order; when prefix lengths differ,
+    // taking the longest sequences first keeps a long one from starting last
+    // and running alone at the end. Launch slot i goes to the sequence of
+    // rank i in (prefix length descending, index ascending), found by every
+    // sequence counting the sequences ahead of it.
+    int32_t* s_len = reinterpret_cast<int32_t*>(smem + OFF_BT);  // reused for the block table below
+    int32_t* s_pick = s_len + kLongestFirstMax;
+    if (tid < p.B) s_len[tid] = p.prefix_len[tid];
+    __syncthreads();
+    if (tid < p.B) {
+      const int32_t mine = s_len[tid];
+      int ahead = 0;
+      for (int u = 0; u < p.B; ++u) {
+        const int32_t o = s_len[u];
+        ahead += (o > mine || (o == mine && u < tid)) ? 1 : 0;
+      }
+      if (ahead == b) *s_pick = tid;
+    }
+    __syncthreads();
+    b = *s_pick;
+    __syncthreads();  // s_len and s_pick are reused
+  }
   const int QH = p.Q * p.H;
   const long long total_rows = (long long)p.B * QH;
   const int32_t* bt = p.block_table + (size_t)b * p.max_pages;
@@ -1175,6 +1202,7 @@ cudaError_t launch_verify_attn_pair(const ddt_attn_dims& d, int n_split, const v
   p.scale_log2 = d.scale * 1.4426950408889634f;
   p.n_rt = (int)((QH + kTM - 1) / kTM);
   p.n_split = n_split;
+  p.longest_first = (d.B > 1 && d.B <= kLongestFirstMax) ? 1 : 0;
   p.block_table = block_table; p.prefix_len = prefix_len;
   p.vis_bits = reinterpret_cast<const unsigned long long*>(vis_bits);
   p.out = static_cast<__nv_bfloat16*>(out);
