@@ -150,6 +150,13 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
                ::: "memory");
 }
+// The same as the first barrier of a kernel, after mbarrier initialisation
+// published by fence.mbarrier_init (release at cluster scope): the arrive
+// itself needs no release, which would wait for the copies already in flight.
+__device__ __forceinline__ void cluster_sync_after_init() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

@@ -347,6 +347,9 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   }
 
   // ---- capacity and page checks: identical decision in all four CTAs ------
+  // each thread's first page index is read together with the prefix length
+  // (the page count depends on it; the first pages are read anyway)
+  const int32_t pg_first = tid < p.max_pages ? bt[tid] : 0;
   const long long L = p.prefix_len[b];
   const long long n_keys = L + p.Q;
   int32_t* s_bt = reinterpret_cast<int32_t*>(smem + OFF_BT);
@@ -357,7 +360,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     const long long kv_pages = p.kv_rows / p.page_size;
     bool badp = false;
     for (long long q = tid; q < n_pages; q += kThreads) {
-      const int32_t pg = bt[q];
+      const int32_t pg = q == tid ? pg_first : bt[q];
       if (q < kBtMax) s_bt[q] = pg;
       if (pg < 0 || pg >= kv_pages) badp = true;
     }
@@ -454,7 +457,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  cluster_sync();  // every barrier and TMEM allocation of the cluster exists before any remote use
+  cluster_sync_after_init();  // every barrier and TMEM allocation of the cluster exists before any remote use
 
   bool failed = false;
   const int rot = nrot > 0 ? (int)(((long long)rt * nrot) / p.n_rt) : 0;
@@ -1064,7 +1067,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                                   : p.part_o + ((long long)sp * total_rows + grow) * kC,
                    stage_s, 1024);
         bulk_commit();
-        bulk_wait0();
+        bulk_wait_read0();
       }
     } else if (warp == 6 && rank == 2) {
       // ---------------- the fused tree build --------------------------------
