@@ -94,10 +94,14 @@ def test_step_deep_long_accepts_15_and_compacts(attn_rows):
 
 
 @pytest.mark.parametrize("q_len,B,L", [(1, 8, 1024), (9, 64, 1024), (33, 1, 8192),
-                                       (65, 8, 8192), (17, 1, 131072), (1, 8, 131072)])
+                                       (65, 8, 8192), (17, 1, 131072), (1, 8, 131072),
+                                       (65, 64, 8192), (33, 8, 65536)])
 def test_step_sweep_points(q_len, B, L, attn_rows):
     w = WL.sweep_point(q_len, B, L)
-    rows = [(0, 0), (B - 1, q_len - 1), (B // 2, q_len // 2)]
+    # rows spread over sequences and over the row tiles (query positions) and
+    # key ranges of the launch
+    rows = sorted({(0, 0), (B - 1, q_len - 1), (B // 2, q_len // 2), (min(1, B - 1), q_len // 4),
+                   (max(B - 2, 0), (3 * q_len) // 4)})
     check_step(w, rows=rows)
 
 
