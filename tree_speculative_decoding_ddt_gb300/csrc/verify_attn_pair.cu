@@ -460,7 +460,12 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync_after_init();  // every barrier and TMEM allocation of the cluster exists before any remote use
 
   bool failed = false;
-  const int rot = nrot > 0 ? (int)(((long long)rt * nrot) / p.n_rt) : 0;
+  // Row tiles of a sequence start their walks up to three tiles apart: close
+  // enough that the tiles one row tile reads are still in L2 for the others
+  // (spreading the starts over the whole prefix cost 2.4x the cache's DRAM
+  // bytes once several long sequences were in flight), far enough that they
+  // do not all ask for the same lines at the start.
+  const int rot = nrot > 0 ? (rt % 4) % nrot : 0;
   auto tile_of = [&](int jj) -> int {
     return (jj < nrot) ? j_begin + (jj + rot) % nrot : j_begin + jj;
   };
@@ -1041,25 +1046,21 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         unsigned char* stage = smem + O_RING + r * kOutStride;
         const uint32_t stage_s = sbase + O_RING + r * kOutStride;
 #pragma unroll 1
-        for (int c = 0; c < 16; c += 2) {
-          uint32_t ov[2][32];
-          tmem_ld32(t_lane + 32 * c, ov[0]);
-          tmem_ld32(t_lane + 32 * (c + 1), ov[1]);
+        for (int c = 0; c < 4; ++c) {  // 128 columns (dims) per TMEM request
+          uint32_t ov[128];
+          tmem_ld128(t_lane + 128 * c, ov);
           tmem_ld_wait();
+          uint4* dst = reinterpret_cast<uint4*>(stage + c * 256);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint4* dst = reinterpret_cast<uint4*>(stage + (c + h) * 64);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              dst[q] = make_uint4(pack_bf16(__uint_as_float(ov[h][8 * q + 0]) * inv_l,
-                                            __uint_as_float(ov[h][8 * q + 1]) * inv_l),
-                                  pack_bf16(__uint_as_float(ov[h][8 * q + 2]) * inv_l,
-                                            __uint_as_float(ov[h][8 * q + 3]) * inv_l),
-                                  pack_bf16(__uint_as_float(ov[h][8 * q + 4]) * inv_l,
-                                            __uint_as_float(ov[h][8 * q + 5]) * inv_l),
-                                  pack_bf16(__uint_as_float(ov[h][8 * q + 6]) * inv_l,
-                                            __uint_as_float(ov[h][8 * q + 7]) * inv_l));
-          }
+          for (int q = 0; q < 16; ++q)
+            dst[q] = make_uint4(pack_bf16(__uint_as_float(ov[8 * q + 0]) * inv_l,
+                                          __uint_as_float(ov[8 * q + 1]) * inv_l),
+                                pack_bf16(__uint_as_float(ov[8 * q + 2]) * inv_l,
+                                          __uint_as_float(ov[8 * q + 3]) * inv_l),
+                                pack_bf16(__uint_as_float(ov[8 * q + 4]) * inv_l,
+                                          __uint_as_float(ov[8 * q + 5]) * inv_l),
+                                pack_bf16(__uint_as_float(ov[8 * q + 6]) * inv_l,
+                                          __uint_as_float(ov[8 * q + 7]) * inv_l));
         }
         fence_proxy_async_smem();
         if (row_ok)
