@@ -26,8 +26,9 @@
  *    DDT_E* code; nothing was enqueued when it is negative (DDT_ELAUNCH: some
  *    earlier kernels of the same call may have been enqueued).
  *  - Problems in the DATA are found on the device and reported per sequence
- *    in `status` (int32[B]) as DDT_ST_* bits; kernels never trap and every
- *    device loop is bounded. ddt_tree_build and ddt_step overwrite status[b];
+ *    in `status` (int32[B]) as DDT_ST_* bits; kernels never trap, every
+ *    device loop is bounded and every wait gives up after about a second
+ *    (DDT_ST_TIMEOUT). ddt_tree_build and ddt_step overwrite status[b];
  *    ddt_verify_attn, ddt_tree_accept and ddt_cache_compact OR their bits in.
  *  - Integer arrays are int32, row-major, densely packed (strides in the
  *    comments). Nodes of a tree are numbered in the order the builder pops
@@ -61,7 +62,7 @@ extern "C" {
 #define DDT_ST_CYCLE 4       /* accept walk would revisit a node (malformed tree) */
 #define DDT_ST_RANGE 8       /* accept path / slot outside the cache; sequence left untouched */
 #define DDT_ST_CAPACITY 16   /* prefix_len + q_len exceeds the sequence's cache capacity */
-#define DDT_ST_TIMEOUT 32    /* a device-side wait ran past its bound; this sequence's outputs are not valid */
+#define DDT_ST_TIMEOUT 32    /* a device-side wait ran past its bound (about 1 s); this sequence's outputs are not valid */
 
 /* ---- element types -------------------------------------------------------- */
 #define DDT_F32 0  /* float32 inputs and outputs; SIMT fp32 arithmetic (exactness path) */
@@ -445,6 +446,16 @@ int ddt_loop_launch(ddt_loop* loop, cudaStream_t stream);
 
 /* Free the graph (deferred by CUDA until a launch in flight completes). */
 int ddt_loop_destroy(ddt_loop* loop);
+
+/* Self-test of the bounded device waits (failure detection; no counterpart on
+ * the source pages). Every kernel of this library waits on mbarrier phases
+ * with a limit of about one second, after which it records DDT_ST_TIMEOUT for
+ * the sequence and leaves instead of hanging. This runs that mechanism alone
+ * in one small kernel on `stream`: result (device, int32[3]) receives
+ * [0] the status of a wait on a phase nothing completes (DDT_ST_TIMEOUT
+ * expected), [1] the status of a wait on a completed phase (0 expected) and
+ * [2] how long the first wait lasted in milliseconds. Takes about a second. */
+int ddt_wait_selftest(int32_t* result, cudaStream_t stream);
 
 /* Static text for a DDT_E* return code. */
 const char* ddt_strerror(int code);

@@ -88,6 +88,7 @@ SIGNATURES = {
     "ddt_loop_create": (ctypes.c_int, [ctypes.POINTER(LoopArgs), ctypes.POINTER(_P)]),
     "ddt_loop_launch": (ctypes.c_int, [_P, _P]),
     "ddt_loop_destroy": (ctypes.c_int, [_P]),
+    "ddt_wait_selftest": (ctypes.c_int, [_P, _P]),
     "ddt_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "ddt_abi_version": (ctypes.c_int, []),
 }
@@ -283,6 +284,15 @@ def ddt_verify_attn_noalloc(q_lat, q_pe, kv_cache, block_table, prefix_len, vis_
                                         _stream(stream))
     _check("ddt_verify_attn_noalloc", rc)
     return out, lse, status
+
+
+def ddt_wait_selftest(stream=None) -> list:
+    """Runs the bounded-wait self-test (about a second); returns [status of a
+    wait nothing completes, status of a completed wait, milliseconds the
+    first wait lasted]."""
+    out = torch.full((3,), -1, dtype=torch.int32, device="cuda")
+    _check("ddt_wait_selftest", load().ddt_wait_selftest(_ptr(out), _stream(stream)))
+    return [int(x) for x in out.cpu()]
 
 
 def ddt_tree_accept(tokens, parents, target_argmax, D: int, status=None, stream=None) -> dict:

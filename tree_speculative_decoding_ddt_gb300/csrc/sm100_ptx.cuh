@@ -2,9 +2,9 @@
 // sm_103a) features the tensor-core verify kernel uses: mbarriers, TMA tile
 // loads, tcgen05 MMA / TMEM, and cluster shared memory.
 //
-// Every wait is bounded: mbar_wait() gives up after kSpinLimit polls and
-// reports false, so a kernel can record an error and leave instead of
-// hanging.
+// Every wait is bounded: mbar_wait() gives up after about a second (by the
+// global timer) and reports false, so a kernel can record an error and leave
+// instead of hanging.
 #pragma once
 
 #include <cuda.h>
@@ -13,7 +13,18 @@
 namespace ddt {
 namespace sm100 {
 
-constexpr uint32_t kSpinLimit = 1u << 26;
+// How long a wait may last before it gives up. A poll of a phase that has not
+// completed suspends the thread for about 4 us on GB300, so the limit is kept
+// by the global timer, not by a count of polls.
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+// Backstop on the polls should the timer not advance.
+constexpr uint32_t kPollLimit = 1u << 28;
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -73,17 +84,26 @@ __device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity)
       : "memory");
   return ok != 0;
 }
-// Wait until the phase with `parity` has completed; false after kSpinLimit polls.
+// Wait until the phase with `parity` has completed; false once about a
+// second has passed without it.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
+  if (mbar_test(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t i = 1; i < kPollLimit; ++i) {
     if (mbar_test(bar, parity)) return true;
-  return false;
+    if ((i & 15u) == 0 && global_ns() - t0 > kWaitLimitNs) break;
+  }
+  return mbar_test(bar, parity);
 }
 // Same, with cluster-scope acquire (for barriers a peer CTA arrives on).
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
+  if (mbar_test_cluster(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t i = 1; i < kPollLimit; ++i) {
     if (mbar_test_cluster(bar, parity)) return true;
-  return false;
+    if ((i & 15u) == 0 && global_ns() - t0 > kWaitLimitNs) break;
+  }
+  return mbar_test_cluster(bar, parity);
 }
 
 // ----------------------------------------------------------------------- TMA
