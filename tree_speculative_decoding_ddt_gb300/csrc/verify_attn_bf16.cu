@@ -402,7 +402,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();  // the peer's barriers are initialised before any remote operation
 
   bool failed = false;
-  const int rot = nrot > 0 ? (int)(((long long)rt * nrot) / p.n_rt) : 0;
+  // row tiles of a sequence start their walks at most three tiles apart (see
+  // the 256-row kernel: spreading the starts over the prefix multiplies the
+  // DRAM bytes once the sequences in flight outgrow L2)
+  const int rot = nrot > 0 ? (rt % 4) % nrot : 0;
   auto tile_of = [&](int jj) -> int {
     return (jj < nrot) ? j_begin + (jj + rot) % nrot : j_begin + jj;
   };
@@ -966,8 +969,8 @@ struct KernelCost {
   double unit_start;  // cycles
   double per_64_keys; // cycles per 64 keys of one unit
 };
-constexpr KernelCost kCost128 = {128, 64, 45000.0, 2300.0};
-constexpr KernelCost kCost256 = {256, 128, 40000.0, 1840.0};
+constexpr KernelCost kCost128 = {128, 64, 45000.0, 2400.0};
+constexpr KernelCost kCost256 = {256, 128, 40000.0, 1750.0};
 constexpr double kMergeBytesPerCycle = 3200.0;  // about 6.6 TB/s at 2.07 GHz
 
 Plan make_plan(const ddt_attn_dims& d, const KernelCost& k, long long per_wave) {
