@@ -92,16 +92,14 @@ def measured_peaks():
 # source whose sha256 is given; reported as null once that source changes.
 MEASURED_TRAFFIC = {
     ("c2_max_budget", 256): ("verify_attn_pair.cu",
-                             "1faffa2d2bd194e71e8c69231e6afb1e6b6b79b3d0bac158d15a7be7c562e30c",
-                             9950976 + 0),
+                             "2f6ebd36a93fe8fcbd3915961d369020262ee53c21102415368e8e73eab5aa53",
+                             9900288 + 0),
+    ("c3_batched_paged", 256): ("verify_attn_pair.cu",
+                                "2f6ebd36a93fe8fcbd3915961d369020262ee53c21102415368e8e73eab5aa53",
+                                452807424 + 56291072),
     ("c4_deep_long", 256): ("verify_attn_pair.cu",
-                            "1faffa2d2bd194e71e8c69231e6afb1e6b6b79b3d0bac158d15a7be7c562e30c",
-                            884251648 + 38849792),
-    # captured with the file at sha 79b0bd59…; since then only k_combine and
-    # the host launcher in that file changed, k_verify_attn_bf16 itself not
-    ("c3_batched_paged", 128): ("verify_attn_bf16.cu",
-                                "81b164da7a004cd7396d10eb949cc8fff33a7ccb455859d9b5e080d028f6f5f1",
-                                502247424 + 62564352),
+                            "2f6ebd36a93fe8fcbd3915961d369020262ee53c21102415368e8e73eab5aa53",
+                            457851904 + 33049344),
 }
 
 
