@@ -460,6 +460,12 @@ int ddt_wait_selftest(int32_t* result, cudaStream_t stream);
 /* Static text for a DDT_E* return code. */
 const char* ddt_strerror(int code);
 
+/* The cudaError_t behind the calling thread's most recent DDT_ELAUNCH
+ * (0 when there was none), and the CUDA runtime's name for such a value
+ * (static text, never NULL). */
+int ddt_last_cuda_error(void);
+const char* ddt_cuda_error_name(int err);
+
 /* Version of this ABI (increments on any incompatible change). */
 int ddt_abi_version(void);
 

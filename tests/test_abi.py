@@ -45,6 +45,10 @@ def test_strerror_and_version(lib):
     assert lib.ddt_strerror(0) == b"ok"
     assert lib.ddt_strerror(-1) == b"invalid argument"
     assert b"unknown" in lib.ddt_strerror(-99)
+    # no launch has failed in this thread; names come from the CUDA runtime
+    assert lib.ddt_last_cuda_error() == 0
+    assert lib.ddt_cuda_error_name(0) == b"cudaSuccess"
+    assert lib.ddt_cuda_error_name(1) == b"cudaErrorInvalidValue"
 
 
 def test_struct_layouts_match_the_header():

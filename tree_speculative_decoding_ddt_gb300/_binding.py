@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(HERE, "libddt.so")
 DDT_F32 = 0
 DDT_BF16 = 1
 DDT_MAX_Q = 128
+DDT_OK, DDT_EINVAL, DDT_EUNSUPPORTED, DDT_ELAUNCH, DDT_EWORKSPACE = 0, -1, -2, -3, -4
 ST_BUDGET_PAD, ST_INPUT, ST_CYCLE, ST_RANGE, ST_CAPACITY, ST_TIMEOUT = 1, 2, 4, 8, 16, 32
 
 
@@ -90,6 +91,8 @@ SIGNATURES = {
     "ddt_loop_destroy": (ctypes.c_int, [_P]),
     "ddt_wait_selftest": (ctypes.c_int, [_P, _P]),
     "ddt_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+    "ddt_last_cuda_error": (ctypes.c_int, []),
+    "ddt_cuda_error_name": (ctypes.c_char_p, [ctypes.c_int]),
     "ddt_abi_version": (ctypes.c_int, []),
 }
 
@@ -116,7 +119,12 @@ def load(path: Optional[str] = None):
 
 def _check(fn: str, rc: int):
     if rc != 0:
-        raise DdtError(fn, rc, load().ddt_strerror(rc).decode())
+        lib = load()
+        text = lib.ddt_strerror(rc).decode()
+        if rc == DDT_ELAUNCH:
+            err = lib.ddt_last_cuda_error()
+            text += f" ({lib.ddt_cuda_error_name(err).decode()}, {err})"
+        raise DdtError(fn, rc, text)
 
 
 def _stream(stream=None) -> int:

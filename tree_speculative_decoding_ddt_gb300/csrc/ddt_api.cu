@@ -54,7 +54,13 @@ int check_compact(int32_t B, int32_t D, int32_t row_bytes, int32_t page_size, in
   return DDT_OK;
 }
 
-inline int launched(cudaError_t e) { return e == cudaSuccess ? DDT_OK : DDT_ELAUNCH; }
+// The CUDA error behind the calling thread's most recent DDT_ELAUNCH.
+thread_local int g_last_cuda_error = 0;
+inline int launched(cudaError_t e) {
+  if (e == cudaSuccess) return DDT_OK;
+  g_last_cuda_error = (int)e;
+  return DDT_ELAUNCH;
+}
 
 size_t attn_workspace(const ddt_attn_dims& d) {
   return d.dtype == DDT_BF16 ? ddt::verify_attn_bf16_workspace(d) : 0;
@@ -120,6 +126,12 @@ int check_verify_attn_args(const ddt_attn_dims* d, const void* q_lat, const void
 extern "C" {
 
 int ddt_abi_version(void) { return kAbiVersion; }
+
+int ddt_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* ddt_cuda_error_name(int err) {
+  return cudaGetErrorName(static_cast<cudaError_t>(err));
+}
 
 const char* ddt_strerror(int code) {
   switch (code) {

@@ -961,16 +961,21 @@ struct Plan {
 // Cost model of a launch, in SM cycles, from cycle traces of both kernels on
 // GB300: a unit (one cluster's rows x key range) costs a fixed start (Q load,
 // instruction fetch, the first tiles through the pipeline, the epilogue) plus
-// its key tiles; units run in waves of `per_wave` clusters; a split key range
-// adds the merge pass, which streams every partial once at HBM speed.
+// its key tiles. The 128-row kernel runs its units in waves of `per_wave`
+// clusters, each paying the whole start; the 256-row kernel keeps `per_wave`
+// clusters resident, each walking its list of units, and a unit that follows
+// another in the same cluster pays only the part of the start that does not
+// overlap the previous unit's end (`unit_next`). A split key range adds the
+// merge pass, which streams every partial once at HBM speed.
 struct KernelCost {
   int rows;           // query rows per tile
   int keys_per_tile;  // keys per step of the key walk
   double unit_start;  // cycles
+  double unit_next;   // cycles, for a unit after another in the same cluster
   double per_64_keys; // cycles per 64 keys of one unit
 };
-constexpr KernelCost kCost128 = {128, 64, 45000.0, 2400.0};
-constexpr KernelCost kCost256 = {256, 128, 40000.0, 1750.0};
+constexpr KernelCost kCost128 = {128, 64, 45000.0, 45000.0, 2400.0};
+constexpr KernelCost kCost256 = {256, 128, 40000.0, 12000.0, 1750.0};
 constexpr double kMergeBytesPerCycle = 3200.0;  // about 6.6 TB/s at 2.07 GHz
 
 Plan make_plan(const ddt_attn_dims& d, const KernelCost& k, long long per_wave) {
@@ -991,11 +996,10 @@ Plan make_plan(const ddt_attn_dims& d, const KernelCost& k, long long per_wave) 
     // tiles of the longest unit (the kernels give every unit but the last
     // one tile more than an even share when the range is split)
     const long long tpu = s > 1 ? (n_tiles + s) / s : n_tiles;
-    const double unit = k.unit_start +
-                        (double)tpu * (double)(k.keys_per_tile / 64) * k.per_64_keys;
+    const double work = (double)tpu * (double)(k.keys_per_tile / 64) * k.per_64_keys;
     const double merge =
         s > 1 ? 3000.0 + (double)(s + 1) * rows_total * 1028.0 / kMergeBytesPerCycle : 0.0;
-    const double cost = waves * unit + merge;
+    const double cost = waves * work + k.unit_start + (waves - 1.0) * k.unit_next + merge;
     if (cost < pl.cost - 1e-9) {
       pl.cost = cost;
       pl.n_split = (int)s;
