@@ -202,12 +202,13 @@ struct Params {
 
 // What warp 0 of a CTA publishes about a unit.
 struct UnitInfo {
-  long long L;  // prefix length
   int b, rt, sp;
   int code;     // DDT_ST_CAPACITY / DDT_ST_RANGE, or 0
+  long long L;  // prefix length
   int pad[2];
 };
-static_assert(sizeof(UnitInfo) * 2 <= 128, "unit info area");
+static_assert(sizeof(UnitInfo) == 32 && offsetof(UnitInfo, L) == 16 && OFF_INFO % 32 == 0,
+              "unit info layout (read by 16- and 8-byte shared loads)");
 
 // Everything else about a unit, derived from its info in the same way by
 // every role.
@@ -254,16 +255,17 @@ __device__ __forceinline__ Unit derive_unit(const Params& p, const UnitInfo& ui)
   u.rot = u.nrot > 0 ? (u.rt % 4) % u.nrot : 0;
   return u;
 }
-// The unit's info re-read from shared memory (a role that needs some of it
-// only after a long loop reads it again instead of holding it in registers).
-__device__ __forceinline__ UnitInfo reload_info(const UnitInfo* pi) {
-  const volatile UnitInfo* v = pi;
+// The unit's info as published in shared memory (read with shared loads from
+// a 32-bit address, so that no role holds a generic pointer to it).
+__device__ __forceinline__ UnitInfo load_info(uint32_t a) {
   UnitInfo ui;
-  ui.L = v->L;
-  ui.b = v->b;
-  ui.rt = v->rt;
-  ui.sp = v->sp;
-  ui.code = v->code;
+  asm volatile("ld.shared.v4.s32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(ui.b), "=r"(ui.rt), "=r"(ui.sp), "=r"(ui.code)
+               : "r"(a)
+               : "memory");
+  uint32_t lo, hi;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(lo), "=r"(hi) : "r"(a + 16) : "memory");
+  ui.L = (long long)(((unsigned long long)hi << 32) | lo);
   return ui;
 }
 
@@ -309,7 +311,8 @@ __device__ void unit_checks(const Params& p, int b, int rt, int sp, int32_t* s_b
   const long long L = p.prefix_len[b];
   const long long n_keys = L + p.Q;
   int code = 0;
-  if (L < 0 || n_keys > (long long)p.max_pages * p.page_size) code = DDT_ST_CAPACITY;
+  if (L < 0 || n_keys > (long long)p.max_pages * p.page_size || n_keys > 0x7fffffffLL)
+    code = DDT_ST_CAPACITY;
   if (code == 0) {
     const long long n_pages = (n_keys + p.page_size - 1) / p.page_size;
     const long long kv_pages = p.kv_rows / p.page_size;
@@ -343,6 +346,38 @@ __device__ void unit_checks(const Params& p, int b, int rt, int sp, int32_t* s_b
   __syncwarp();
 }
 
+__device__ __forceinline__ int lds_s32(uint32_t a) {
+  int v;
+  asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts_s32(uint32_t a, int v) {
+  asm volatile("st.shared.s32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long lds_u64(uint32_t a) {
+  unsigned long long v;
+  asm volatile("ld.shared.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts_u64(uint32_t a, unsigned long long v) {
+  asm volatile("st.shared.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
+}
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts_f32(uint32_t a, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+__device__ __forceinline__ float2 lds_f32x2(uint32_t a) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts_f32x2(uint32_t a, float x, float y) {
+  asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(x), "f"(y) : "memory");
+}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -461,9 +496,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + N_BARS * 8);
-  auto bar = [&](int i) { return smem_u32(bars + i); };
+  auto bar = [&](int i) { return sbase + OFF_BAR + 8u * (uint32_t)i; };
 
   const uint32_t rank = cluster_rank();
   const bool s_side = rank < 2;
@@ -582,10 +616,13 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   bool failed = false;
   // unit i of this cluster, as published by warp 0: 1 ready, 0 no such unit,
   // -1 the wait gave up
+  // the number of units of this cluster: one per full round, and one in the
+  // last, partial round when its position there exists
+  const int n_mine = (int)(U / G) + (unit_id(cl, G, (int)(U / G)) < U ? 1 : 0);
   auto take_unit = [&](int i, Unit& u) -> int {
-    if (unit_id(cl, G, i) >= U) return 0;
+    if (i >= n_mine) return 0;
     if (!mbar_wait(bar(B_INFO + (i & 1)), (i >> 1) & 1)) return -1;
-    u = derive_unit(p, infos[i & 1]);
+    u = derive_unit(p, load_info(sbase + OFF_INFO + (i & 1) * sizeof(UnitInfo)));
     return 1;
   };
   // one thread per consuming warp
@@ -616,7 +653,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         unit_coords(p, order, uid, &b, &rt, &sp);
         unit_checks(p, b, rt, sp, s_bt_of(i), infos + (i & 1), lane);
         if (lane == 0) mbar_arrive(bar(B_INFO + (i & 1)));
-        const Unit u = derive_unit(p, infos[i & 1]);
+        const Unit u = derive_unit(p, load_info(sbase + OFF_INFO + (i & 1) * sizeof(UnitInfo)));
         if (u.nt == 0) {
           write_empty_warp(p, u, rank, lane);
           if (u.code && u.rt == 0 && u.sp == 0 && rank == 0 && lane == 0)
@@ -811,8 +848,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       const int r = qd * 32 + lane;
       const uint32_t t_lane = tmem + ((uint32_t)(qd * 32) << 16);
       const int W = (p.Q + 63) >> 6;
-      float* hand = reinterpret_cast<float*>(smem + S_XCH);  // [row]: running max handoff
-      float* fin = hand + kHM;                               // [group][row][2]: (m, l) at the end
+      const uint32_t hand = sbase + S_XCH;     // float [row]: running max handoff
+      const uint32_t fin = hand + kHM * 4;     // float [group][row][2]: (m, l) at the end
       const uint32_t msg_peer0 = map_peer(sbase + O_MSG, rank + 2);
       const uint32_t pfull_peer0 = map_peer(bar(B_P_FULL), rank + 2);
       const uint32_t bar_in = 2 + 2 * qd + g;         // handoff to this group
@@ -825,9 +862,11 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       // bit v the parity of the building units of ancestor-word buffer v, [3]
       // tiles this group took in the earlier units (uses of S buffer g), [4]
       // P blocks of the earlier units.
-      volatile int* cnt = reinterpret_cast<volatile int*>(smem + OFF_CNT) + 8 * (warp - 2);
+      const uint32_t cnt = sbase + OFF_CNT + 32 * (warp - 2);  // int32 [8]
+      auto cnt_ld = [&](int k) { return lds_s32(cnt + 4 * k); };
+      auto cnt_st = [&](int k, int v) { sts_s32(cnt + 4 * k, v); };
       if (lane == 0)
-        for (int k = 0; k < 5; ++k) cnt[k] = 0;
+        for (int k = 0; k < 5; ++k) cnt_st(k, 0);
       __syncwarp();
       for (int i = 0; !failed; ++i) {
         Unit u;
@@ -839,7 +878,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (u.nt == 0) {
           __syncwarp();
-          if (i == 0 && lane == 0) cnt[1] = 1;
+          if (i == 0 && lane == 0) cnt_st(1, 1);
           __syncwarp();
           if (lane == 0) release_unit(i);
           continue;
@@ -847,18 +886,23 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         const int lr = u.rt * kTM + half * kHM + r;
         const bool row_ok = lr < QH;
         const int qi = row_ok ? lr / p.H : 0;
-        unsigned long long vis0 = 0ull, vis1 = 0ull;
-        bool vis_ready = !p.fuse;
+        // The row's ancestor words sit in the unit's buffer of S_VIS (filled by
+        // the fused build, or here from the caller's vis_bits: each thread
+        // writes the words of its own query, which it alone reads back), and
+        // are read where a block holds tree keys.
+        const uint32_t vis_row = sbase + S_VIS + (cnt_ld(0) & 1) * kVisBuf + qi * kMaxW * 8;
         if (!p.fuse && row_ok) {
           const unsigned long long* vb = p.vis_bits + ((size_t)u.b * p.Q + qi) * W;
-          vis0 = vb[0];
-          if (W > 1) vis1 = vb[1];
+          sts_u64(vis_row, vb[0]);
+          sts_u64(vis_row + 8, W > 1 ? vb[1] : 0ull);
         }
+        const int Lk = (int)u.L;       // prefix keys
+        const int nk_all = (int)u.n_keys;
         // q_lat row r -> TMEM columns [0,256) (bf16 pairs); group g moves
         // chunks 4g .. 4g + 3, which its stage of the ring holds. The MMAs of
         // the previous unit have completed: both groups saw their last S
         // buffers filled before the previous unit's end.
-        const bool q_ok = __all_sync(0xffffffffu, mbar_wait(bar(B_Q_FULL + g), cnt[1] & 1));
+        const bool q_ok = __all_sync(0xffffffffu, mbar_wait(bar(B_Q_FULL + g), cnt_ld(1) & 1));
         if (q_ok) {
           tc_fence_after();
           const unsigned char* qrow = smem + S_RING + g * kTileK + r * 128;
@@ -902,7 +946,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
           float x[128];  // raw scores q.k of the tile's 128 keys
           if (ok) {
             ok = __all_sync(0xffffffffu,
-                            mbar_wait_cluster(bar(B_S_FULL + g), (cnt[3] + (jj >> 1)) & 1));
+                            mbar_wait_cluster(bar(B_S_FULL + g), (cnt_ld(3) + (jj >> 1)) & 1));
             tc_fence_after();
             uint32_t sa[128];  // the whole S row in one request, so the buffer is freed soon
             tmem_ld128(t_lane + kTmemS + g * kBS, sa);
@@ -915,29 +959,23 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kb = 0; kb < 2; ++kb) {
               const int blk = 2 * tile + kb;
-              const long long t0 = (long long)blk * kBK;
+              const int t0 = blk * kBK;
               unsigned long long m = ~0ull;  // visible keys of the block
               if (blk >= u.n_blocks) {
                 m = 0ull;  // the phantom block
-              } else if (t0 + kBK > u.L) {
-                if (!vis_ready) {
-                  const int vb = cnt[0] & 1;
+              } else if (t0 + kBK > Lk) {
+                if (p.fuse) {
+                  const int vb = cnt_ld(0) & 1;
                   ok = ok && __all_sync(0xffffffffu, mbar_wait_cluster(bar(B_TREE + vb),
-                                                                        (cnt[2] >> vb) & 1));
-                  if (row_ok) {
-                    const unsigned long long* vw = reinterpret_cast<const unsigned long long*>(
-                                                       smem + S_VIS + vb * kVisBuf) +
-                                                   qi * kMaxW;
-                    vis0 = vw[0];
-                    vis1 = vw[1];
-                  }
-                  vis_ready = true;
+                                                                        (cnt_ld(2) >> vb) & 1));
                 }
+                const unsigned long long vis0 = row_ok ? lds_u64(vis_row) : 0ull;
+                const unsigned long long vis1 = row_ok ? lds_u64(vis_row + 8) : 0ull;
                 // key k is slot t0 + k; slots below L are prefix, slot L + t is
                 // tree slot t (bit t of vis1:vis0), slots from n_keys on do not exist
-                const int np = (int)max(0ll, u.L - t0);
-                const int off = (int)(t0 - u.L);
-                const int nk = (int)min(64ll, u.n_keys - t0);
+                const int np = max(0, Lk - t0);
+                const int off = t0 - Lk;
+                const int nk = min(64, nk_all - t0);
                 unsigned long long tm;
                 if (off < 0) tm = vis0 << (-off);
                 else if (off == 0) tm = vis0;
@@ -969,7 +1007,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
           // running max after the previous tile, from the other group
           if (jj > 0) {
             asm volatile("bar.sync %0, 64;" ::"r"(bar_in) : "memory");
-            m_run = hand[r];
+            m_run = lds_f32(hand + 4 * r);
           }
           // lazy rescale: the reference max moves only when the row max passes it
           // by 8 (a factor 2^8); O on the peer is then multiplied by `factor`
@@ -982,7 +1020,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
             m_run = mt;
           }
           if (jj + 1 < u.nt) {
-            hand[r] = m_run;
+            sts_f32(hand + 4 * r, m_run);
             asm volatile("bar.arrive %0, 64;" ::"r"(bar_out) : "memory");
           }
           // Exponentials, P blocks and their copies. The group barriers run
@@ -1000,7 +1038,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kb = 0; kb < 2; ++kb) {
             if (2 * tile + kb >= u.n_blocks) continue;
-            const int msg_g = cnt[4] + 2 * jj + kb;  // the P block's number in the cluster's stream
+            const int msg_g = cnt_ld(4) + 2 * jj + kb;  // the P block's number in the cluster's stream
             const int ss = msg_g % kStageSlots;
             if (ok && msg_g >= kStageSlots)
               ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar(B_STAGE_FREE + ss),
@@ -1055,19 +1093,18 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
 
         // ---- the unit's end: the row sum over both groups, lse here, 1/l to
         // the O-CTA (through one of two buffers, by unit parity) ------------
-        const Unit ue = derive_unit(p, reload_info(infos + (i & 1)));
-        fin[(g * kHM + r) * 2 + 0] = m_l;
-        fin[(g * kHM + r) * 2 + 1] = l_run;
+        const Unit ue = derive_unit(p, load_info(sbase + OFF_INFO + (i & 1) * sizeof(UnitInfo)));
+        sts_f32x2(fin + 8 * (g * kHM + r), m_l, l_run);
         asm volatile("bar.sync %0, 64;" ::"r"(12 + qd) : "memory");
         bool fin_ok = bar1_and(!failed, 256);
-        const int kq = cnt[0];
+        const int kq = cnt_ld(0);
         const int fb = kq & 1;
         if (g == 0 && fin_ok && kq >= 2)  // the O-CTA has read this buffer's previous 1/l
           fin_ok = __all_sync(0xffffffffu,
                               mbar_wait_cluster(bar(B_FIN_FREE + fb), ((kq >> 1) - 1) & 1));
         if (g == 0 && fin_ok) {
-          const float ma = fin[r * 2 + 0], la = fin[r * 2 + 1];
-          const float mb2 = fin[(kHM + r) * 2 + 0], lb = fin[(kHM + r) * 2 + 1];
+          const float2 fa = lds_f32x2(fin + 8 * r), fb2 = lds_f32x2(fin + 8 * (kHM + r));
+          const float ma = fa.x, la = fa.y, mb2 = fb2.x, lb = fb2.y;
           const float mf = fmaxf(ma, mb2);
           float l_tot = 0.f;
           if (la != 0.f) l_tot += la * ex2(ma - mf);
@@ -1097,11 +1134,11 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) release_unit(i);
         __syncwarp();
         if (lane == 0) {
-          if (ue.builds) cnt[2] = cnt[2] ^ (1 << (kq & 1));
-          cnt[0] = kq + 1;
-          cnt[1] = cnt[1] + 1;
-          cnt[3] = cnt[3] + (ue.nt - g + 1) / 2;
-          cnt[4] = cnt[4] + ue.n_msgs;
+          if (ue.builds) cnt_st(2, cnt_ld(2) ^ (1 << (kq & 1)));
+          cnt_st(0, kq + 1);
+          cnt_st(1, cnt_ld(1) + 1);
+          cnt_st(3, cnt_ld(3) + (ue.nt - g + 1) / 2);
+          cnt_st(4, cnt_ld(4) + ue.n_msgs);
         }
         __syncwarp();
       }
@@ -1126,7 +1163,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         unit_coords(p, order, uid, &b, &rt, &sp);
         unit_checks(p, b, rt, sp, s_bt_of(i), infos + (i & 1), lane);
         if (lane == 0) mbar_arrive(bar(B_INFO + (i & 1)));
-        const Unit u = derive_unit(p, infos[i & 1]);
+        const Unit u = derive_unit(p, load_info(sbase + OFF_INFO + (i & 1) * sizeof(UnitInfo)));
         if (u.nt == 0) {
           write_empty_warp(p, u, rank, lane);
           continue;
@@ -1716,12 +1753,13 @@ cudaError_t launch_verify_attn_pair(const ddt_attn_dims& d, int n_split, const v
   cudaError_t e = ensure_smem_limit(k_verify_attn_pair, (int)kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
   // at most as many clusters as are resident at once; each walks its list of
-  // units. DDT_PAIR_CLUSTERS (a positive count) lowers the cap, so that a small
-  // launch can run many units per cluster.
+  // units. DDT_PAIR_CLUSTERS (a positive count) sets the number of clusters
+  // instead (at most one per unit): a small launch can then run many units per
+  // cluster, or a large one one unit per cluster.
   const long long units = (long long)d.B * p.n_rt * n_split;
   long long cap = verify_attn_pair_clusters_per_wave();
   const char* env = getenv("DDT_PAIR_CLUSTERS");
-  if (env != nullptr && atoll(env) > 0 && (cap <= 0 || atoll(env) < cap)) cap = atoll(env);
+  if (env != nullptr && atoll(env) > 0) cap = atoll(env);
   const long long clusters = cap > 0 && units > cap ? cap : units;
   k_verify_attn_pair<<<(unsigned)(clusters * 4), kThreads, kSmemBytes, stream>>>(
       tm_k, tm_v, tm_ql, tm_qp, tm_o, p);
