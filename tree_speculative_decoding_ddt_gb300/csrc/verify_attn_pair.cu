@@ -18,8 +18,9 @@
 //   * ranks 0, 1 (the S pair) hold Q rows [0,128) and [128,256) of the tile:
 //     q_lat in TMEM (256 columns), q_pe in shared memory (16 KB). S is taken
 //     over 128-key tiles: each S-CTA loads one 64-key half of the tile (64
-//     keys x 576 dims, 72 KB) and the pair MMA (issued by rank 0; N = 128, so
-//     36 MMA instructions per 128 keys) writes S for its 128 rows x all 128
+//     keys x 576 dims, 72 KB, one TMA request) and the pair MMA (issued by
+//     rank 0; N = 128, so 36 MMA instructions per 128 keys) writes S for its
+//     128 rows x all 128
 //     keys into each CTA's TMEM (two 128-column buffers). Eight softmax warps
 //     per CTA take two threads per row, one per 64-key half; each half ships
 //     its P block (bf16, 16 KB) plus per-row rescale factors to the O-CTA of
@@ -84,6 +85,12 @@ constexpr int kStageSlots = 3;  // S-CTA: outgoing P blocks (free once copied)
 constexpr int kMsgSlots = 4;    // O-CTA: incoming P blocks (free once PV has read them)
 
 constexpr int kChunks = (kC + kR) / 64;                   // 9 chunks of 64 dims
+// Key loads per 64-key half, each released to the producer when its MMAs are
+// done. Splitting the half into 3 or 9 loads, so that the next tile's first
+// chunks land early, measured slower at c4 (1557 and 1944 us against 1487):
+// the per-request cost of the smaller loads outweighs the earlier start.
+constexpr int kKGroups = 1;
+constexpr int kGroupChunks = kChunks / kKGroups;          // chunks per key load
 constexpr uint32_t kKChunk = kBK * 128;                   // 64 keys x 128 B
 constexpr uint32_t kTileK = kChunks * kKChunk;            // an S-CTA's key half: 72 KB
 constexpr uint32_t kVChunk = kBK * 128;                   // 64 keys x 128 B
@@ -138,10 +145,11 @@ static_assert(kLongestFirstMax <= kThreads, "one thread per sequence ranks the l
 
 enum Bar {
   // S-CTAs
-  B_RING_FULL = 0,                        // +stage; this CTA's key half landed
-  B_RING_PEER = B_RING_FULL + kStagesK,   // +stage; rank 0: rank 1's key half landed (relay)
-  B_RING_EMPTY = B_RING_PEER + kStagesK,  // +stage; both (pair MMA commit)
-  B_S_FULL = B_RING_EMPTY + kStagesK,     // +buffer; both (pair MMA commit)
+  // key ring barriers are per chunk group of a stage: index stage * kKGroups + group
+  B_RING_FULL = 0,                                   // this CTA's group landed
+  B_RING_PEER = B_RING_FULL + kStagesK * kKGroups,   // rank 0: rank 1's group landed (relay)
+  B_RING_EMPTY = B_RING_PEER + kStagesK * kKGroups,  // both: the MMAs of the group are done
+  B_S_FULL = B_RING_EMPTY + kStagesK * kKGroups,     // +buffer; both (pair MMA commit)
   B_S_EMPTY = B_S_FULL + 2,               // +buffer; rank 0: its 4 warps of one group + rank 1's relay
   B_S_READ = B_S_EMPTY + 2,               // +buffer; rank 1: its 4 warps of one group read S
   B_Q_FULL = B_S_READ + 2,                // +half; q_lat dims [256h, 256h + 256) landed (h = 0: and q_pe)
@@ -538,7 +546,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   // ---- setup ---------------------------------------------------------------
   if (tid == 0) {
     if (s_side) {
-      for (int s = 0; s < kStagesK; ++s) {
+      for (int s = 0; s < kStagesK * kKGroups; ++s) {
         mbar_init(bar(B_RING_FULL + s), 1);
         mbar_init(bar(B_RING_PEER + s), 1);
         mbar_init(bar(B_RING_EMPTY + s), 1);
@@ -673,7 +681,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
             // of q_pe and of the q_lat in TMEM), a Q half moved to TMEM, or a
             // Q load that was never used
             for (int s = 0; s < 2 && ok; ++s)
-              ok = (keyl >> s) & 1 ? mbar_wait_cluster(bar(B_RING_EMPTY + s), ((rpar >> s) & 1) ^ 1)
+              ok = (keyl >> s) & 1 ? mbar_wait_cluster(bar(B_RING_EMPTY + s * kKGroups + kKGroups - 1),
+                                                       ((rpar >> s) & 1) ^ 1)
                    : (qused >> s) & 1 ? mbar_wait(bar(B_Q_LOCAL + s), (lqpar >> s) & 1)
                                       : mbar_wait(bar(B_Q_FULL + s), (qn - 1) & 1);
             if (ok) {
@@ -692,16 +701,28 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
           const int32_t* s_bt = s_bt_of(i);
           for (int uu = 0; uu < u.nt && ok; ++uu) {
             const int slot = uu & 1;
-            // the stage is free once its half of q_lat has left it, then after
-            // the MMAs of the tile two back
-            ok = uu < 2 ? mbar_wait(bar(B_Q_LOCAL + slot), kq & 1)
-                        : mbar_wait_cluster(bar(B_RING_EMPTY + slot), ((rpar >> slot) & 1) ^ 1);
-            if (!ok) break;
-            mbar_expect_tx(bar(B_RING_FULL + slot), kTileK);
+            // The stage is free once its half of q_lat has left it; later a
+            // chunk of the stage is reloaded as soon as the MMAs of the tile
+            // two back have read it, so the next tile's keys are in place
+            // long before its MMAs start.
+            if (uu < 2 && !mbar_wait(bar(B_Q_LOCAL + slot), kq & 1)) {
+              ok = 0;
+              break;
+            }
             int blk = 2 * tile_of(u, uu) + half;
             if (blk >= u.n_blocks) blk -= 1;  // the phantom half: the other half's rows
-            tma_load_3d(sbase + S_RING + slot * kTileK, &tm_k, 0, (int)block_row(p, u, s_bt, blk), 0,
-                        bar(B_RING_FULL + slot));
+            const int krow = (int)block_row(p, u, s_bt, blk);
+            const int gb0 = slot * kKGroups;
+            for (int q = 0; q < kKGroups; ++q) {
+              if (uu >= 2 &&
+                  !mbar_wait_cluster(bar(B_RING_EMPTY + gb0 + q), ((rpar >> slot) & 1) ^ 1)) {
+                ok = 0;
+                break;
+              }
+              mbar_expect_tx(bar(B_RING_FULL + gb0 + q), kGroupChunks * kKChunk);
+              tma_load_3d(sbase + S_RING + slot * kTileK + q * kGroupChunks * kKChunk, &tm_k, 0,
+                          krow, q * kGroupChunks, bar(B_RING_FULL + gb0 + q));
+            }
             rpar ^= 1u << slot;
             keyl |= 1u << slot;
           }
@@ -712,8 +733,13 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       // nothing may land after the CTAs leave
       if (lane == 0) {
         for (int s = 0; s < 2; ++s) {
-          const bool ok = (keyl >> s) & 1 ? mbar_wait(bar(B_RING_FULL + s), ((rpar >> s) & 1) ^ 1)
-                                          : mbar_wait(bar(B_Q_FULL + s), (qn - 1) & 1);
+          bool ok = true;
+          if ((keyl >> s) & 1) {
+            for (int q = 0; q < kKGroups; ++q)
+              ok = mbar_wait(bar(B_RING_FULL + s * kKGroups + q), ((rpar >> s) & 1) ^ 1) && ok;
+          } else {
+            ok = mbar_wait(bar(B_Q_FULL + s), (qn - 1) & 1);
+          }
           if (!ok) failed = true;
           if (((tused >> s) & 1) && !mbar_wait_cluster(bar(B_TREE + s), ((tpar >> s) & 1) ^ 1))
             failed = true;
@@ -743,31 +769,44 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
               }
-              if (!mbar_wait(bar(B_RING_FULL + sb), n_iss & 1) ||
-                  !mbar_wait_cluster(bar(B_RING_PEER + sb), n_iss & 1)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
               const uint32_t d = tmem + kTmemS + sb * kBS;
               const uint32_t st = sbase + S_RING + sb * kTileK;
-#pragma unroll
-              for (int c = 0; c < kC / 64; ++c) {
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                  const uint64_t bd = smem_desc(st + c * kKChunk + kk * 32, 16, 1024, kSwizzle128B);
-                  umma_pair_bf16_ts(d, tmem + kTmemQ + 32 * c + 8 * kk, bd, kIdescS,
-                                    (c | kk) ? 1u : 0u);
+              const int gb0 = sb * kKGroups;
+              // group by group: each is waited for (here and on rank 1) and
+              // released to the producer as soon as its MMAs are done
+#pragma unroll 1
+              for (int q = 0; q < kKGroups && ok; ++q) {
+                if (!mbar_wait(bar(B_RING_FULL + gb0 + q), n_iss & 1) ||
+                    !mbar_wait_cluster(bar(B_RING_PEER + gb0 + q), n_iss & 1)) {
+                  ok = false;
+                  break;
                 }
-              }
+                tc_fence_after();
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t ad = smem_desc(sbase + S_QPE + kk * 32, 16, 1024, kSwizzle128B);
-                const uint64_t bd =
-                    smem_desc(st + (kC / 64) * kKChunk + kk * 32, 16, 1024, kSwizzle128B);
-                umma_pair_bf16(d, ad, bd, kIdescS, 1u);
+                for (int cc = 0; cc < kGroupChunks; ++cc) {
+                  const int c = q * kGroupChunks + cc;
+                  if (c < kC / 64) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                      const uint64_t bd =
+                          smem_desc(st + c * kKChunk + kk * 32, 16, 1024, kSwizzle128B);
+                      umma_pair_bf16_ts(d, tmem + kTmemQ + 32 * c + 8 * kk, bd, kIdescS,
+                                        (c | kk) ? 1u : 0u);
+                    }
+                  } else {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                      const uint64_t ad =
+                          smem_desc(sbase + S_QPE + kk * 32, 16, 1024, kSwizzle128B);
+                      const uint64_t bd =
+                          smem_desc(st + c * kKChunk + kk * 32, 16, 1024, kSwizzle128B);
+                      umma_pair_bf16(d, ad, bd, kIdescS, 1u);
+                    }
+                  }
+                }
+                umma_pair_commit(bar(B_RING_EMPTY + gb0 + q), kMaskS);
               }
-              umma_pair_commit(bar(B_RING_EMPTY + sb), kMaskS);
+              if (!ok) break;
               umma_pair_commit(bar(B_S_FULL + sb), kMaskS);
               ++n_iss;
             }
@@ -796,9 +835,11 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
           bool ok = t > 0;
           for (int uu = 0; ok && uu < u.nt; ++uu) {
             const int slot = uu & 1;
-            ok = mbar_wait(bar(B_RING_FULL + slot), (par >> slot) & 1);
+            for (int q = 0; ok && q < kKGroups; ++q) {
+              ok = mbar_wait(bar(B_RING_FULL + slot * kKGroups + q), (par >> slot) & 1);
+              if (ok) mbar_arrive_cluster_relaxed(peer0 + 8 * (slot * kKGroups + q));
+            }
             par ^= 1u << slot;
-            if (ok) mbar_arrive_cluster_relaxed(peer0 + 8 * slot);
           }
           if (!ok) {
             failed = true;
@@ -1638,7 +1679,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 }
 
 // Keys: the cache as {64 dims, rows, 9 chunks} (strides: row, 128 B); a box of
-// {64, 64, 9} lands as nine 64-key x 128-byte swizzled chunks (8 KB each).
+// {64, 64, kGroupChunks} at chunk c lands as that many 64-key x 128-byte
+// swizzled chunks (8 KB each); a 64-key half of an S tile is kKGroups such
+// requests.
 // Values: the c_kv part as {64 dims, rows, 4 chunks, 2 halves} (strides: row,
 // 128 B, 512 B); a box of {64, 64, 2, 2} at chunk 2h holds dims
 // [128h, 128h + 128) and [256 + 128h, 256 + 128h + 128) as four 8 KB chunks.
@@ -1657,7 +1700,7 @@ bool encode_maps(CUtensorMap* mk, CUtensorMap* mv, CUtensorMap* ml, CUtensorMap*
   {
     cuuint64_t dims[3] = {64, kv_rows, (cuuint64_t)kChunks};
     cuuint64_t str[2] = {(cuuint64_t)(kC + kR) * 2, 128};
-    cuuint32_t box[3] = {64, (cuuint32_t)kBK, (cuuint32_t)kChunks};
+    cuuint32_t box[3] = {64, (cuuint32_t)kBK, (cuuint32_t)kGroupChunks};  // a group of chunks
     if (fn(mk, bf, 3, const_cast<void*>(kv), dims, str, box, e4, il, sw, l2, oob) != CUDA_SUCCESS)
       return false;
   }
