@@ -4,6 +4,7 @@ else: a short, reproducible launch sequence for a profiler.
     python -m tree_speculative_decoding_ddt_gb300.cases stress [--B 65536] [--reps 2]
     python -m tree_speculative_decoding_ddt_gb300.cases attn --config c4 [--reps 2]
     python -m tree_speculative_decoding_ddt_gb300.cases step --config c2 [--reps 2]
+    python -m tree_speculative_decoding_ddt_gb300.cases next --config c3 [--reps 2]
 
 ``stress``: the build / accept / compaction stress case (B sequences with the
 batched workload's drafter shape, D 8, K 4, budget 16, V 163840; a bf16 cache
@@ -15,6 +16,12 @@ ddt_cache_compact, in that order, and the statuses are checked at the end.
 ``attn`` / ``step``: the verify attention (ddt_verify_attn) or the whole step
 (ddt_step) on a named workload (c1..c4, or a sweep point q<len>_b<batch>_l<prefix>)
 with its seeded inputs, ``reps`` times on one stream.
+
+``next``: the calls beside the verify step on a named workload's shapes, each
+``reps`` times: ddt_target_argmax over B*Q x V logits, ddt_drafter_topk over
+B*D x V logits (K of the workload), and ddt_rope_append of the workload's
+q_pe and B*Q new latents into its cache at the tree's positions L + depth
+(logits and latents drawn on the device from a seeded generator).
 """
 from __future__ import annotations
 
@@ -105,15 +112,52 @@ def run_workload(name: str, reps: int, whole_step: bool) -> None:
     print(f"{'step' if whole_step else 'attn'} case: {w.name}, {reps} repetitions")
 
 
+def run_next(name: str, reps: int) -> None:
+    import numpy as np
+    import torch
+
+    from . import _binding as DB
+    from . import workloads as WL
+    w = _workload(name)
+    batch = WL.make_batch(w, latents=False)
+    lay = batch.layout
+    dev = torch.device("cuda", torch.cuda.current_device())
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234)
+    ldt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
+    logits = (torch.randn((w.B * w.Q, w.V), generator=gen, device=dev) * w.logit_std).to(ldt)
+    dl = (torch.randn((w.B * w.D, w.V), generator=gen, device=dev) * w.logit_std).to(ldt)
+    q_pe = torch.randn((w.B, w.Q, w.H, w.R), generator=gen, device=dev).to(ldt)
+    kv_new = torch.randn((w.B, w.Q, w.C + w.R), generator=gen, device=dev).to(ldt)
+    kv = torch.zeros((lay.total_rows, w.C + w.R), dtype=ldt, device=dev)
+    tree = DB.ddt_tree_build(torch.from_numpy(batch.topk_logp).to(dev), i32(batch.topk_ids),
+                             i32(batch.root_tok), w.budget, w.V)
+    bt, L = i32(lay.block_table), i32(batch.prefix_len)
+    st = torch.zeros((w.B,), dtype=torch.int32, device=dev)
+    am = tk = q_out = None
+    for _ in range(reps):
+        am = DB.ddt_target_argmax(logits, out=am)
+        tk = DB.ddt_drafter_topk(dl, w.K, out=tk)
+        q_out, _ = DB.ddt_rope_append(q_pe, kv_new, kv, bt, L, tree["depths"], lay.page_size,
+                                      q_out=q_out, status=st)
+    torch.cuda.synchronize()
+    if int(st.abs().sum()) != 0:
+        raise SystemExit(f"{name}: rope_append status reports errors: {st.cpu().numpy()}")
+    print(f"next case: {w.name}, {reps} repetitions")
+
+
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
-    ap.add_argument("case", choices=["stress", "attn", "step"])
+    ap.add_argument("case", choices=["stress", "attn", "step", "next"])
     ap.add_argument("--B", type=int, default=65536)
     ap.add_argument("--config", default="c4")
     ap.add_argument("--reps", type=int, default=2)
     a = ap.parse_args(argv)
     if a.case == "stress":
         run_stress(a.B, a.reps)
+    elif a.case == "next":
+        run_next(a.config, a.reps)
     else:
         run_workload(a.config, a.reps, a.case == "step")
     return 0

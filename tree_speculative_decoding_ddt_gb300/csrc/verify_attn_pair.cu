@@ -138,6 +138,8 @@ static_assert(kMsgBytes <= kMsgStride && kMsgBytes % 16 == 0, "message size");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 static_assert(O_OUT % 1024 == 0 && O_OUT + 4 * 2 * kOutBox <= O_RING + 3 * kTileV,
               "the output is staged in value stage 2");
+static_assert(4 * 8 * kOutBox <= kStagesV * kTileV,
+              "a cluster's last unit stages all its output boxes in the value ring");
 static_assert(S_QPE % 1024 == 0, "q_pe is an MMA operand");
 static_assert(S_VIS % 16 == 0 && kVisBuf % 16 == 0, "ancestor words are bulk-copied");
 static_assert(offsetof(tb::Smem, anc) % 16 == 0, "ancestor words are bulk-copied");
@@ -622,11 +624,11 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync_after_init();  // every barrier and TMEM allocation of the cluster exists before any remote use
 
   bool failed = false;
-  // unit i of this cluster, as published by warp 0: 1 ready, 0 no such unit,
-  // -1 the wait gave up
   // the number of units of this cluster: one per full round, and one in the
   // last, partial round when its position there exists
   const int n_mine = (int)(U / G) + (unit_id(cl, G, (int)(U / G)) < U ? 1 : 0);
+  // unit i of this cluster, as published by warp 0: 1 ready, 0 no such unit,
+  // -1 the wait gave up
   auto take_unit = [&](int i, Unit& u) -> int {
     if (i >= n_mine) return 0;
     if (!mbar_wait(bar(B_INFO + (i & 1)), (i >> 1) & 1)) return -1;
@@ -1213,7 +1215,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           const int32_t* s_bt = s_bt_of(i);
           for (int m = 0; m < u.n_msgs; ++m) {
-            const int stage = m & (kStagesV - 1);
+            const int stage = m % kStagesV;
             if (((vused >> stage) & 1) &&
                 !mbar_wait_cluster(bar(B_HALF_EMPTY + stage), ((vpar >> stage) & 1) ^ 1)) {
               ok = 0;
@@ -1237,7 +1239,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
           // keys past the end of the sequence in the last block: their values are
           // zeroed so that 0 * (whatever the page holds) cannot turn into NaN
           const int m = u.n_msgs - 1;
-          const int stage = m & (kStagesV - 1);
+          const int stage = m % kStagesV;
           const long long t0 = (long long)msg_block(u, m) * kBK;
           if (t0 + kBK > u.n_keys) {
             // the stage parities live in lane 0, which issued the loads
@@ -1296,7 +1298,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
               const int mg = gb + jj;
               const int mb = mg % kMsgSlots;
               const uint32_t ph = (mg / kMsgSlots) & 1;
-              const int stage = jj & (kStagesV - 1);
+              const int stage = jj % kStagesV;
               const uint32_t vph = (vpar >> stage) & 1;
               vpar ^= 1u << stage;
               if (!mbar_wait(bar(B_P_FULL + mb), ph) || !mbar_wait_cluster(bar(B_P_PEER + mb), ph)) {
@@ -1390,7 +1392,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
           if (t == 0) break;
           bool ok = t > 0;
           for (int m = 0; ok && u.nt > 0 && m < u.n_msgs; ++m) {
-            const int stage = m & (kStagesV - 1);
+            const int stage = m % kStagesV;
             ok = mbar_wait(bar(B_HALF_FULL + stage), (par >> stage) & 1);
             par ^= 1u << stage;
             if (ok) mbar_arrive_cluster_relaxed(peer2 + 8 * stage);
@@ -1519,6 +1521,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
             // writes its rows one by one.
             const int lr0 = u.rt * kTM + half * kHM + qd * 32;
             const bool boxed = lr0 + 32 <= QH;
+            const bool last_unit = i == n_mine - 1;
             const long long orow = p.n_split == 1 ? 0 : (long long)u.sp * total_rows;
             const int y0 = (int)(orow + row0 + qd * 32);
             __nv_bfloat16* dst_row =
@@ -1541,8 +1544,15 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                   const int box = 2 * c + h;
-                  const uint32_t bx = box_w + (uint32_t)(box & 1) * kOutBox;
-                  if (box >= 2) {  // the box's store two back has read its staging
+                  // The cluster's last unit has the whole value ring to itself
+                  // (no value tile follows): each box gets its own staging, so
+                  // no store waits for another. Otherwise two boxes per warp in
+                  // value stage 2, each reused once the store two back has
+                  // read it.
+                  const uint32_t bx = last_unit
+                                          ? sbase + O_RING + ((uint32_t)qd * 8 + box) * kOutBox
+                                          : box_w + (uint32_t)(box & 1) * kOutBox;
+                  if (!last_unit && box >= 2) {
                     if (lane == 0) bulk_wait_read1();
                     __syncwarp();
                   }
