@@ -63,6 +63,7 @@ extern "C" {
 #define DDT_ST_RANGE 8       /* accept path / slot outside the cache; sequence left untouched */
 #define DDT_ST_CAPACITY 16   /* prefix_len + q_len exceeds the sequence's cache capacity */
 #define DDT_ST_TIMEOUT 32    /* a device-side wait ran past its bound (about 1 s); this sequence's outputs are not valid */
+#define DDT_ST_CHECK 64      /* (library built with DDT_CHECKS) a device bounds check failed; the access was skipped or clamped */
 
 /* ---- element types -------------------------------------------------------- */
 #define DDT_F32 0  /* float32 inputs and outputs; SIMT fp32 arithmetic (exactness path) */
@@ -459,6 +460,19 @@ int ddt_wait_selftest(int32_t* result, cudaStream_t stream);
 
 /* Static text for a DDT_E* return code. */
 const char* ddt_strerror(int code);
+
+/* Debug-build bounds checks (SURVEY's safety plan; no counterpart on the
+ * source pages). A library built with -DDDT_CHECKS (libddt_checks.so) tests
+ * every computed global row, page and TMA coordinate before the access it
+ * guards; a failing check skips the access (or clamps a TMA coordinate to a
+ * valid row, so that no barrier is left waiting), counts the failure, keeps
+ * the id of the first failing site, and ORs DDT_ST_CHECK into the sequence's
+ * status where the call has one. This reads and resets the counts: it
+ * returns 1 in such a library (0 in the release library, whose checks
+ * compile to nothing), with n_failed the number of failed checks since the
+ * last call and first_site the id of the earliest (file * 100 + site; 0 if
+ * none). Synchronises the device. */
+int ddt_debug_checks(int* n_failed, int* first_site);
 
 /* The cudaError_t behind the calling thread's most recent DDT_ELAUNCH
  * (0 when there was none), and the CUDA runtime's name for such a value

@@ -27,3 +27,18 @@ def attn_rows(request, monkeypatch):
     tiles on paired SMs), forced through DDT_VERIFY_ATTN_ROWS."""
     monkeypatch.setenv("DDT_VERIFY_ATTN_ROWS", request.param)
     return int(request.param)
+
+
+@pytest.fixture(autouse=True)
+def _no_failed_bounds_checks(request):
+    """Under DDT_LIB=checks (the library built with device bounds checks),
+    every GPU test also asserts that no check failed during it."""
+    yield
+    if os.environ.get("DDT_LIB") != "checks" or request.node.get_closest_marker("gpu") is None:
+        return
+    import torch
+    from tree_speculative_decoding_ddt_gb300 import _binding
+    torch.cuda.synchronize()
+    built, n_failed, first = _binding.debug_checks()
+    assert built, "DDT_LIB=checks but the loaded library was built without DDT_CHECKS"
+    assert n_failed == 0, f"{n_failed} device bounds checks failed (first at site {first})"

@@ -51,6 +51,22 @@ def test_strerror_and_version(lib):
     assert lib.ddt_cuda_error_name(1) == b"cudaErrorInvalidValue"
 
 
+def test_debug_checks_entry_point(lib):
+    import ctypes as C
+    n, first = C.c_int(7), C.c_int(7)
+    # the release library reports no checks and zero counts (no device needed)
+    assert lib.ddt_debug_checks(C.byref(n), C.byref(first)) == 0
+    assert (n.value, first.value) == (0, 0)
+    dbg = os.path.join(os.path.dirname(B.LIB_PATH), "libddt_checks.so")
+    if not os.path.exists(dbg):
+        pytest.skip("libddt_checks.so not built")
+    d = C.CDLL(dbg)
+    d.ddt_debug_checks.restype = C.c_int
+    d.ddt_debug_checks.argtypes = [C.c_void_p, C.c_void_p]
+    assert d.ddt_debug_checks(C.byref(n), C.byref(first)) == 1
+    assert n.value == 0
+
+
 def test_struct_layouts_match_the_header():
     assert ctypes.sizeof(B.TreeDims) == 20
     assert ctypes.sizeof(B.AttnDims) == 48

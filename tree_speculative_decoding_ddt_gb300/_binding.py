@@ -16,13 +16,16 @@ from typing import Optional
 import torch
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libddt.so")
+# DDT_LIB=checks selects the debug build (device bounds checks recording a
+# status, see ddt_debug_checks); anything else, the release library.
+LIB_PATH = os.path.join(HERE, "libddt_checks.so" if os.environ.get("DDT_LIB") == "checks"
+                        else "libddt.so")
 
 DDT_F32 = 0
 DDT_BF16 = 1
 DDT_MAX_Q = 128
 DDT_OK, DDT_EINVAL, DDT_EUNSUPPORTED, DDT_ELAUNCH, DDT_EWORKSPACE = 0, -1, -2, -3, -4
-ST_BUDGET_PAD, ST_INPUT, ST_CYCLE, ST_RANGE, ST_CAPACITY, ST_TIMEOUT = 1, 2, 4, 8, 16, 32
+ST_BUDGET_PAD, ST_INPUT, ST_CYCLE, ST_RANGE, ST_CAPACITY, ST_TIMEOUT, ST_CHECK = 1, 2, 4, 8, 16, 32, 64
 
 
 class DdtError(RuntimeError):
@@ -92,6 +95,7 @@ SIGNATURES = {
     "ddt_wait_selftest": (ctypes.c_int, [_P, _P]),
     "ddt_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "ddt_last_cuda_error": (ctypes.c_int, []),
+    "ddt_debug_checks": (ctypes.c_int, [_P, _P]),
     "ddt_cuda_error_name": (ctypes.c_char_p, [ctypes.c_int]),
     "ddt_abi_version": (ctypes.c_int, []),
 }
@@ -115,6 +119,14 @@ def load(path: Optional[str] = None):
         fn.argtypes = args
     _lib = lib
     return lib
+
+
+def debug_checks():
+    """(built with checks, failed checks since the last call, first failing
+    site) from ddt_debug_checks; reading resets the counts."""
+    n, first = ctypes.c_int(0), ctypes.c_int(0)
+    built = load().ddt_debug_checks(ctypes.byref(n), ctypes.byref(first))
+    return bool(built), n.value, first.value
 
 
 def _check(fn: str, rc: int):

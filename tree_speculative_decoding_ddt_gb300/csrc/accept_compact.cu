@@ -31,6 +31,7 @@
 #include "ddt_internal.cuh"
 
 namespace ddt {
+DDT_CHECKS_FILE(accept)
 namespace {
 
 constexpr int kThreads = 256;
@@ -243,8 +244,13 @@ __global__ void __launch_bounds__(kThreads, kCompact ? 4 : 8)
             first = off[k];
           }
         const int i = r - first;
-        v[j] = *reinterpret_cast<const uint4*>(a.kv + s_src[w][i] + 16 * c);
-        to[j] = s_dst[w][i] + 16 * c;
+        // both 16-byte pieces inside the cache (the slots were checked per row)
+        const long long kv_bytes = a.kv_rows * (long long)a.row_bytes;
+        if (DDT_GUARD(s_src[w][i] + 16 * c + 16 <= kv_bytes && s_dst[w][i] + 16 * c + 16 <= kv_bytes,
+                      501, nullptr)) {
+          v[j] = *reinterpret_cast<const uint4*>(a.kv + s_src[w][i] + 16 * c);
+          to[j] = s_dst[w][i] + 16 * c;
+        }
       }
       c += step_c;
       r += step_r;

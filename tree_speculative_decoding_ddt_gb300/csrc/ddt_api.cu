@@ -129,6 +129,29 @@ int ddt_abi_version(void) { return kAbiVersion; }
 
 int ddt_last_cuda_error(void) { return g_last_cuda_error; }
 
+int ddt_debug_checks(int* n_failed, int* first_site) {
+  int (*const readers[])(int*) = {ddt::checks_read_pair,  ddt::checks_read_bf16,
+                                  ddt::checks_read_f32,   ddt::checks_read_build,
+                                  ddt::checks_read_accept, ddt::checks_read_rope,
+                                  ddt::checks_read_topk,  ddt::checks_read_argmax};
+  int total = 0, first = 0;
+  for (auto rd : readers) {
+    int f = 0;
+    const int n = rd(&f);
+    if (n > 0) {
+      total += n;
+      if (first == 0) first = f;
+    }
+  }
+  if (n_failed) *n_failed = total;
+  if (first_site) *first_site = first;
+#ifdef DDT_CHECKS
+  return 1;
+#else
+  return 0;
+#endif
+}
+
 const char* ddt_cuda_error_name(int err) {
   return cudaGetErrorName(static_cast<cudaError_t>(err));
 }

@@ -71,6 +71,47 @@ struct TreeFuse {
 // Largest candidate table (min(D,budget) x min(K,budget)) the fused build stages.
 constexpr int kFuseMaxCand = 1024;
 
+// ---- debug-build bounds checks ------------------------------------------------
+// With -DDDT_CHECKS, DDT_GUARD(cond, site, status) is false when cond fails,
+// after counting the failure in the file's device counters (count, first
+// failing site) and OR-ing DDT_ST_CHECK into *status (status may be null).
+// Without the flag it is the constant true and cond is not evaluated. Each
+// .cu file that uses it names its counters once with DDT_CHECKS_FILE(name);
+// checks_read_<name>() reads and resets them (host, synchronising).
+#ifdef DDT_CHECKS
+__device__ __forceinline__ bool ddt_check_failed(int* chk, int site, int32_t* status) {
+  if (atomicAdd(&chk[0], 1) == 0) chk[1] = site;
+  if (status != nullptr) atomicOr(status, DDT_ST_CHECK);
+  return false;
+}
+#define DDT_GUARD(cond, site, status) ((cond) ? true : ::ddt::ddt_check_failed(g_chk, (site), (status)))
+#define DDT_CHECKS_FILE(name)                                            \
+  static __device__ int g_chk[2];                                        \
+  int checks_read_##name(int* first) {                                   \
+    int h[2] = {0, 0};                                                   \
+    const int z[2] = {0, 0};                                             \
+    if (cudaMemcpyFromSymbol(h, g_chk, sizeof(h)) != cudaSuccess) h[0] = -1; \
+    cudaMemcpyToSymbol(g_chk, z, sizeof(z));                             \
+    *first = h[1];                                                       \
+    return h[0];                                                         \
+  }
+#else
+#define DDT_GUARD(cond, site, status) true
+#define DDT_CHECKS_FILE(name)        \
+  int checks_read_##name(int* first) { \
+    *first = 0;                      \
+    return 0;                        \
+  }
+#endif
+int checks_read_pair(int* first);
+int checks_read_bf16(int* first);
+int checks_read_f32(int* first);
+int checks_read_build(int* first);
+int checks_read_accept(int* first);
+int checks_read_rope(int* first);
+int checks_read_topk(int* first);
+int checks_read_argmax(int* first);
+
 // B. verify attention, bf16 tcgen05 path. With `fuse`, vis_bits is not read:
 // the kernel builds the tree itself and status must be zero on entry.
 size_t verify_attn_bf16_workspace(const ddt_attn_dims& d);

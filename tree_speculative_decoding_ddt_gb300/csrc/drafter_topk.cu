@@ -29,6 +29,7 @@
 #include "sm100_ptx.cuh"
 
 namespace ddt {
+DDT_CHECKS_FILE(topk)
 namespace {
 
 using namespace sm100;
@@ -267,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
   const long long per = (((V + ncta - 1) / ncta) + E::kPerVec - 1) / E::kPerVec * E::kPerVec;
   const long long c0 = min(V, (long long)crank * per);
   const long long c1 = min(V, c0 + per);
+  if (tid == 0) (void)DDT_GUARD(c0 >= 0 && c0 <= c1 && c1 <= V, 701, nullptr);
   TopList<KT> tl;
   tl.clear();
   Lse ls;

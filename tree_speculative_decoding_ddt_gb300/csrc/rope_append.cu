@@ -26,6 +26,7 @@
 #include "ddt_internal.cuh"
 
 namespace ddt {
+DDT_CHECKS_FILE(rope)
 namespace {
 
 constexpr int kThreads = 128;
@@ -216,7 +217,8 @@ __global__ void __launch_bounds__(kThreads) k_rope_append(const RopeArgs a) {
 
   // ---- the latent row to cache slot L + t: latent part copied, rope part turned
   const long long slot = L + t;
-  const long long row = (long long)bt[slot / a.page_size] * a.page_size + slot % a.page_size;
+  long long row = (long long)bt[slot / a.page_size] * a.page_size + slot % a.page_size;
+  if (!DDT_GUARD(row >= 0 && row < a.kv_rows, 601, a.status + b)) return;
   T* dst = static_cast<T*>(a.kv) + row * CR;
   if (a.vec) {
     if (tid < n_lat) reinterpret_cast<uint4*>(dst)[tid] = lat_v;

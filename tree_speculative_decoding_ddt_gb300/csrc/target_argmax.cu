@@ -23,6 +23,7 @@
 #include "sm100_ptx.cuh"
 
 namespace ddt {
+DDT_CHECKS_FILE(argmax)
 namespace {
 
 using namespace sm100;
@@ -117,6 +118,7 @@ __global__ void __launch_bounds__(kThreads)
   const long long per = (((V + ncta - 1) / ncta) + E::kPerVec - 1) / E::kPerVec * E::kPerVec;
   const long long c0 = min(V, (long long)crank * per);
   const long long c1 = min(V, c0 + per);
+  if (tid == 0) (void)DDT_GUARD(c0 >= 0 && c0 <= c1 && c1 <= V, 801, nullptr);
   Best bt;
   if (vec) {
     const long long nv = (c1 - c0) / E::kPerVec;

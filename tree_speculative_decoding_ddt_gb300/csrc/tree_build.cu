@@ -5,6 +5,7 @@
 #include "tree_build_warp.cuh"
 
 namespace ddt {
+DDT_CHECKS_FILE(build)
 namespace {
 
 constexpr int kWarpsPerCta = 4;  // sequences per CTA, one warp each
@@ -32,6 +33,8 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) k_tree_build(
   const int32_t st = tb::write_warp(S, b, budget + 1, n, bad, tokens, parents, depths, vis_bits,
                                     vis, first_child, next_sibling, n_nodes_out);
   if ((threadIdx.x & 31) == 0) status[b] = st;
+  // the pop loop yields the root and at most `budget` nodes
+  if ((threadIdx.x & 31) == 0) (void)DDT_GUARD(n >= 1 && n <= budget + 1, 401, status + b);
 }
 
 }  // namespace

@@ -52,6 +52,7 @@
 #include "tree_build_warp.cuh"
 
 namespace ddt {
+DDT_CHECKS_FILE(bf16)
 namespace {
 
 using namespace sm100;
@@ -412,8 +413,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   auto krow_of = [&](int jj) -> long long {
     const long long t0 = (long long)tile_of(jj) * kBN;
     const long long pi = t0 / p.page_size;
+    if (!DDT_GUARD(pi >= 0 && pi < p.max_pages, 201, p.status + b)) return 0;
     const int32_t pg = pi < kBtMax ? reinterpret_cast<const int32_t*>(smem + OFF_BT)[pi] : bt[pi];
-    return (long long)pg * p.page_size + t0 % p.page_size;
+    const long long row = (long long)pg * p.page_size + t0 % p.page_size;
+    // a key tile must lie inside the cache (the TMA is clamped to row 0 otherwise)
+    return DDT_GUARD(row >= 0 && row + kBN <= p.kv_rows, 202, p.status + b) ? row : 0;
   };
 
   if (rank == 0) {
@@ -488,7 +492,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       unsigned long long vis0 = 0ull, vis1 = 0ull;
       bool vis_ready = !p.fuse;  // a fused build delivers them before the first tree tile
       if (!p.fuse && row_ok) {
-        const unsigned long long* vb = p.vis_bits + ((size_t)b * p.Q + qi) * W;
+        const unsigned long long* vb =
+            p.vis_bits + ((size_t)b * p.Q + (DDT_GUARD(qi < p.Q, 203, p.status + b) ? qi : 0)) * W;
         vis0 = vb[0];
         if (W > 1) vis1 = vb[1];
       }
@@ -653,7 +658,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const float lse_v =
               live ? (m_run + __log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
           if (p.n_split == 1) {
-            if (p.lse) p.lse[grow] = lse_v;
+            if (p.lse && DDT_GUARD(grow < total_rows, 204, p.status + b)) p.lse[grow] = lse_v;
           } else {
             p.part_lse[(long long)sp * total_rows + grow] = lse_v;
           }
@@ -839,7 +844,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         fence_proxy_async_smem();
-        if (row_ok)
+        if (row_ok && DDT_GUARD(grow < total_rows, 205, p.status + b))
           bulk_s2g(p.n_split == 1 ? p.out + grow * kC
                                   : p.part_o + ((long long)sp * total_rows + grow) * kC,
                    stage_s, 1024);

@@ -17,6 +17,7 @@
 #include "ddt_internal.cuh"
 
 namespace ddt {
+DDT_CHECKS_FILE(f32)
 namespace {
 
 constexpr int kHeads = 8;
@@ -93,8 +94,9 @@ __global__ void __launch_bounds__(kHeads * 32) k_verify_attn_f32(
     for (int j = warp; j < kTile; j += kHeads) {
       const long long slot = t0 + j;
       float* dst = kv_s + j * ld;
-      if (slot < n_keys) {
-        const float* src = kv + slot_row(bt, page_size, slot) * CR;
+      const long long srow = slot < n_keys ? slot_row(bt, page_size, slot) : 0;
+      if (slot < n_keys && DDT_GUARD(srow >= 0 && srow < kv_rows, 301, status + b)) {
+        const float* src = kv + srow * CR;
         for (int d = lane; d < CR; d += 32) dst[d] = src[d];
       } else {
         for (int d = lane; d < CR; d += 32) dst[d] = 0.f;

@@ -68,6 +68,7 @@
 #include "tree_build_warp.cuh"
 
 namespace ddt {
+DDT_CHECKS_FILE(pair)
 namespace {
 
 using namespace sm100;
@@ -290,8 +291,11 @@ __device__ __forceinline__ long long block_row(const Params& p, const Unit& u, c
                                                int blk) {
   const long long t0 = (long long)blk * kBK;
   const long long pi = t0 / p.page_size;
+  if (!DDT_GUARD(pi >= 0 && pi < p.max_pages, 101, p.status + u.b)) return 0;
   const int32_t pg = pi < kBtMax ? s_bt[pi] : p.block_table[(size_t)u.b * p.max_pages + pi];
-  return (long long)pg * p.page_size + t0 % p.page_size;
+  const long long row = (long long)pg * p.page_size + t0 % p.page_size;
+  // a 64-key block must lie inside the cache (the TMA is clamped to row 0 otherwise)
+  return DDT_GUARD(row >= 0 && row + kBK <= p.kv_rows, 102, p.status + u.b) ? row : 0;
 }
 
 // Unit i of cluster c among G clusters: units are numbered longest first
@@ -933,7 +937,9 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         // the fused build, or here from the caller's vis_bits: each thread
         // writes the words of its own query, which it alone reads back), and
         // are read where a block holds tree keys.
-        const uint32_t vis_row = sbase + S_VIS + (cnt_ld(0) & 1) * kVisBuf + qi * kMaxW * 8;
+        const uint32_t vis_row =
+            sbase + S_VIS + (cnt_ld(0) & 1) * kVisBuf +
+            (DDT_GUARD(qi < p.Q, 103, p.status + u.b) ? qi : 0) * kMaxW * 8;
         if (!p.fuse && row_ok) {
           const unsigned long long* vb = p.vis_bits + ((size_t)u.b * p.Q + qi) * W;
           sts_u64(vis_row, vb[0]);
@@ -1157,7 +1163,8 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
           const long long grow = (long long)ue.b * QH + lre;
           if (lre < QH) {
             const float lse_v = live ? (mf + __log2f(l_tot)) * 0.69314718055994530942f : -INFINITY;
-            if (p.n_split == 1) {
+            if (!DDT_GUARD(grow < total_rows, 104, p.status + ue.b)) {
+            } else if (p.n_split == 1) {
               if (p.lse) p.lse[grow] = lse_v;
             } else {
               p.part_lse[(long long)ue.sp * total_rows + grow] = lse_v;
@@ -1570,11 +1577,13 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                   fence_proxy_async_smem();
                   __syncwarp();
                   if (lane == 0) {
-                    tma_store_2d(&tm_o, bx, 64 * box, y0);
+                    if (DDT_GUARD((long long)y0 + 32 <= (p.n_split == 1 ? 1 : p.n_split) * total_rows,
+                                  105, p.status + u.b))
+                      tma_store_2d(&tm_o, bx, 64 * box, y0);
                     bulk_commit();
                   }
                 }
-              } else if (row_ok) {
+              } else if (row_ok && DDT_GUARD(row0 + r < total_rows, 106, p.status + u.b)) {
                 uint4* dst = reinterpret_cast<uint4*>(dst_row + 128 * c);
 #pragma unroll
                 for (int q = 0; q < 16; ++q)
