@@ -888,51 +888,25 @@ __device__ void combine_row(long long row, long long total_rows, int n_split,
                             const float* __restrict__ part_lse, __nv_bfloat16* __restrict__ out,
                             float* __restrict__ lse_out) {
   const int lane = threadIdx.x & 31;
-  // Up to eight partials at a time: their lse and this lane's 16 dims are all
-  // requested before any is used (one memory round trip instead of two).
-  constexpr int kBatch = 8;
   float m = -INFINITY;
+  for (int s = 0; s < n_split; ++s) m = fmaxf(m, part_lse[(long long)s * total_rows + row]);
   float acc[16];
 #pragma unroll
   for (int k = 0; k < 16; ++k) acc[k] = 0.f;
   float wsum = 0.f;
-  for (int s0 = 0; s0 < n_split; s0 += kBatch) {
-    float ls[kBatch];
-    uint4 v[kBatch][2];
-#pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
-      const int s = s0 + j;
-      if (s < n_split) {
-        ls[j] = part_lse[(long long)s * total_rows + row];
-        const uint4* src =
-            reinterpret_cast<const uint4*>(part_o + ((long long)s * total_rows + row) * kC) +
-            lane * 2;
-        v[j][0] = src[0];
-        v[j][1] = src[1];
-      } else {
-        ls[j] = -INFINITY;
-      }
-    }
-    // the running reference max moves to the batch's max; earlier sums rescale
-    float mb = m;
-#pragma unroll
-    for (int j = 0; j < kBatch; ++j) mb = fmaxf(mb, ls[j]);
-    if (mb == -INFINITY) continue;
-    if (mb != m) {
-      const float r = m == -INFINITY ? 0.f : expf(m - mb);
-      wsum *= r;
-#pragma unroll
-      for (int k = 0; k < 16; ++k) acc[k] *= r;
-      m = mb;
-    }
-#pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
-      if (ls[j] == -INFINITY) continue;
-      const float w = expf(ls[j] - m);
+  if (m != -INFINITY) {
+    for (int s = 0; s < n_split; ++s) {
+      const float ls = part_lse[(long long)s * total_rows + row];
+      if (ls == -INFINITY) continue;
+      const float w = expf(ls - m);
       wsum += w;
+      const uint4* src =
+          reinterpret_cast<const uint4*>(part_o + ((long long)s * total_rows + row) * kC) +
+          lane * 2;
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        const uint32_t wv[4] = {v[j][q].x, v[j][q].y, v[j][q].z, v[j][q].w};
+        const uint4 v = src[q];
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[e]));
