@@ -295,6 +295,15 @@ __device__ __forceinline__ void umma_pair_commit(uint32_t bar, uint16_t cta_mask
       "h"(cta_mask)
       : "memory");
 }
+// Copy a matrix of 128 rows x 256 bits (16 bf16 of K per row), described by
+// the shared-memory descriptor `src`, into TMEM lanes 0..127, columns
+// [col, col + 8) of `taddr`, in both CTAs of the pair (each from its own shared
+// memory at the same offset). Asynchronous and issued by one thread like a
+// pair MMA: the MMAs that thread issues later read it, and a commit from that
+// thread tracks its completion.
+__device__ __forceinline__ void tmem_cp_pair_128x256b(uint32_t taddr, uint64_t src) {
+  asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(src) : "memory");
+}
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
                                             int w, uint32_t bar) {
   asm volatile(

@@ -16,7 +16,9 @@
 // SM, so S and O still live on different SMs, and each side is now a pair of
 // SMs running one M = 256 MMA:
 //   * ranks 0, 1 (the S pair) hold Q rows [0,128) and [128,256) of the tile:
-//     q_lat in TMEM (256 columns), q_pe in shared memory (16 KB). S is taken
+//     q_lat in TMEM (256 columns: staged through the key ring by TMA and
+//     copied in by the MMA issuer with tcgen05.cp), q_pe in shared memory
+//     (16 KB). S is taken
 //     over 128-key tiles: each S-CTA loads one 64-key half of the tile (64
 //     keys x 576 dims, 72 KB, one TMA request) and the pair MMA (issued by
 //     rank 0; N = 128, so 36 MMA instructions per 128 keys) writes S for its
@@ -156,8 +158,9 @@ enum Bar {
   B_S_EMPTY = B_S_FULL + 2,               // +buffer; rank 0: its 4 warps of one group + rank 1's relay
   B_S_READ = B_S_EMPTY + 2,               // +buffer; rank 1: its 4 warps of one group read S
   B_Q_FULL = B_S_READ + 2,                // +half; q_lat dims [256h, 256h + 256) landed (h = 0: and q_pe)
-  B_Q_LOCAL = B_Q_FULL + 2,               // +half; this CTA's group h has moved its half to TMEM
-  B_Q_TMEM = B_Q_LOCAL + 2,               // rank 0: all q_lat of both CTAs in TMEM (8 + 8 warps)
+  B_Q_PEER = B_Q_FULL + 2,                // rank 0: both of rank 1's q_lat halves landed (relay)
+  B_Q_LOCAL = B_Q_PEER + 1,               // +half; both: the half has been copied into TMEM (pair commit)
+  B_Q_TMEM = B_Q_LOCAL + 2,               // rank 0: all q_lat of both CTAs in TMEM (commit)
   B_P_FREE = B_Q_TMEM + 1,                // +O-CTA slot; both (PV commit from rank 2)
   B_STAGE_FREE = B_P_FREE + kMsgSlots,    // +staging slot; the O-CTA saw the copy land
   B_TREE = B_STAGE_FREE + kStageSlots,    // +buffer; ancestor words of the fused build landed
@@ -562,13 +565,14 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(bar(B_S_EMPTY + s), 5);
         mbar_init(bar(B_S_READ + s), 4);
         mbar_init(bar(B_Q_FULL + s), 1);
-        mbar_init(bar(B_Q_LOCAL + s), 4);
+        mbar_init(bar(B_Q_LOCAL + s), 1);
         mbar_init(bar(B_TREE + s), 1);
         mbar_init(bar(B_FIN_FREE + s), 4);
       }
       for (int s = 0; s < kMsgSlots; ++s) mbar_init(bar(B_P_FREE + s), 1);
       for (int s = 0; s < kStageSlots; ++s) mbar_init(bar(B_STAGE_FREE + s), 1);
-      mbar_init(bar(B_Q_TMEM), 16);  // used on rank 0
+      mbar_init(bar(B_Q_TMEM), 1);  // used on rank 0
+      mbar_init(bar(B_Q_PEER), 1);  // used on rank 0
       mbar_init(bar(B_MMA_DONE), 2);
     } else {
       for (int s = 0; s < kStagesV; ++s) {
@@ -759,6 +763,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         const int sb = warp == 1 ? 0 : 1;
         int kq = 0, n_iss = 0;  // tiles this issuer has issued (uses of its stage and S buffer)
+        int qn = 0;             // Q loads consumed (the first unit's counts even without tiles)
         for (int i = 0; !failed; ++i) {
           Unit u;
           const int t = take_unit(i, u);
@@ -767,9 +772,39 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
             failed = true;
             break;
           }
+          if (u.nt == 0 && i == 0) qn = 1;
           if (u.nt > 0) {
-            bool ok = mbar_wait_cluster(bar(B_Q_TMEM), kq & 1);
-            tc_fence_after();
+            bool ok;
+            if (sb == 0) {
+              // The unit's q_lat, staged in both stages of the key ring of both
+              // CTAs, goes to TMEM columns [0, 256) (bf16 pairs, row = lane)
+              // through the tensor pipe, ahead of the first MMAs, which see it
+              // in issue order; each stage is handed back to its producer once
+              // its copies are done. The previous unit's MMAs, the last readers
+              // of those columns, completed before the producers loaded this Q.
+              ok = mbar_wait(bar(B_Q_FULL + 0), qn & 1) && mbar_wait(bar(B_Q_FULL + 1), qn & 1) &&
+                   mbar_wait_cluster(bar(B_Q_PEER), kq & 1);
+              tc_fence_after();
+              if (ok) {
+#pragma unroll 1
+                for (int s = 0; s < 2; ++s) {
+                  const uint32_t qs = sbase + S_RING + s * kTileK;
+#pragma unroll
+                  for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                      tmem_cp_pair_128x256b(
+                          tmem + kTmemQ + 32 * (4 * s + c) + 8 * kk,
+                          smem_desc(qs + c * (kHM * 128) + kk * 32, 16, 1024, kSwizzle128B));
+                  umma_pair_commit(bar(B_Q_LOCAL + s), kMaskS);
+                }
+                umma_pair_commit(bar(B_Q_TMEM), 0x1);
+              }
+            } else {
+              ok = mbar_wait_cluster(bar(B_Q_TMEM), kq & 1);
+              tc_fence_after();
+            }
+            ++qn;
             for (int jj = sb; jj < u.nt && ok; jj += 2) {
               if (n_iss > 0 && !mbar_wait_cluster(bar(B_S_EMPTY + sb), (n_iss - 1) & 1)) {
                 ok = false;
@@ -828,17 +863,25 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         if (!mbar_wait(bar(B_MMA_DONE), 0)) failed = true;
       }
     } else if (rank == 1 && warp == 10) {
-      // relay: this CTA's key half of a tile has landed -> rank 0's MMA issuers
-      // (each CTA's tile loads complete on its own barrier; a load that signals
-      // the peer's barrier directly slows this CTA's outgoing P copies)
+      // relay: this CTA's Q, then each key half of a tile, has landed -> rank
+      // 0's MMA issuers (each CTA's tile loads complete on its own barrier; a
+      // load that signals the peer's barrier directly slows this CTA's
+      // outgoing P copies)
       if (lane == 0) {
         const uint32_t peer0 = map_peer(bar(B_RING_PEER), 0);
         uint32_t par = 0;  // bit s: parity of the key halves of stage s
+        int qn = 0;        // Q loads consumed (the first unit's counts even without tiles)
         for (int i = 0; !failed; ++i) {
           Unit u;
           const int t = take_unit(i, u);
           if (t == 0) break;
           bool ok = t > 0;
+          if (ok && u.nt == 0 && i == 0) qn = 1;
+          if (ok && u.nt > 0) {
+            ok = mbar_wait(bar(B_Q_FULL + 0), qn & 1) && mbar_wait(bar(B_Q_FULL + 1), qn & 1);
+            if (ok) mbar_arrive_cluster_relaxed(map_peer(bar(B_Q_PEER), 0));
+            ++qn;
+          }
           for (int uu = 0; ok && uu < u.nt; ++uu) {
             const int slot = uu & 1;
             for (int q = 0; ok && q < kKGroups; ++q) {
@@ -904,16 +947,15 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t bar_grp = 10 + g;                // the group's four warps
       const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
       // Counters carried from unit to unit, kept in shared memory (the tile
-      // loop needs every register): [0] units with key tiles so far, [1] Q
-      // loads so far (the first unit's counts even when it has no tiles), [2]
-      // bit v the parity of the building units of ancestor-word buffer v, [3]
-      // tiles this group took in the earlier units (uses of S buffer g), [4]
+      // loop needs every register): [0] units with key tiles so far, [1] bit
+      // v the parity of the building units of ancestor-word buffer v, [2]
+      // tiles this group took in the earlier units (uses of S buffer g), [3]
       // P blocks of the earlier units.
       const uint32_t cnt = sbase + OFF_CNT + 32 * (warp - 2);  // int32 [8]
       auto cnt_ld = [&](int k) { return lds_s32(cnt + 4 * k); };
       auto cnt_st = [&](int k, int v) { sts_s32(cnt + 4 * k, v); };
       if (lane == 0)
-        for (int k = 0; k < 5; ++k) cnt_st(k, 0);
+        for (int k = 0; k < 4; ++k) cnt_st(k, 0);
       __syncwarp();
       for (int i = 0; !failed; ++i) {
         Unit u;
@@ -924,8 +966,6 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         }
         if (u.nt == 0) {
-          __syncwarp();
-          if (i == 0 && lane == 0) cnt_st(1, 1);
           __syncwarp();
           if (lane == 0) release_unit(i);
           continue;
@@ -947,41 +987,6 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         }
         const int Lk = (int)u.L;       // prefix keys
         const int nk_all = (int)u.n_keys;
-        // q_lat row r -> TMEM columns [0,256) (bf16 pairs); group g moves
-        // chunks 4g .. 4g + 3, which its stage of the ring holds. The MMAs of
-        // the previous unit have completed: both groups saw their last S
-        // buffers filled before the previous unit's end.
-        const bool q_ok = __all_sync(0xffffffffu, mbar_wait(bar(B_Q_FULL + g), cnt_ld(1) & 1));
-        if (q_ok) {
-          tc_fence_after();
-          const unsigned char* qrow = smem + S_RING + g * kTileK + r * 128;
-#pragma unroll 1
-          for (int c = 4 * g; c < 4 * g + 4; ++c) {
-            uint32_t v[32];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const uint4 x = *reinterpret_cast<const uint4*>(qrow + (c - 4 * g) * (kHM * 128) +
-                                                               ((q ^ (r & 7)) << 4));
-              v[4 * q + 0] = x.x;
-              v[4 * q + 1] = x.y;
-              v[4 * q + 2] = x.z;
-              v[4 * q + 3] = x.w;
-            }
-            tmem_st32(t_lane + kTmemQ + 32 * c, v);
-          }
-          tmem_st_wait();
-        }
-        fence_proxy_async_smem();  // the ring is refilled by TMA after this
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(bar(B_Q_LOCAL + g));  // this stage of the ring may take key tiles
-          // rank 0's MMA issuers need the q_lat of both CTAs in TMEM (the
-          // arrive passes on stores to TMEM that have completed here)
-          if (rank == 0) mbar_arrive(bar(B_Q_TMEM));
-          else mbar_arrive_cluster_relaxed(map_peer(bar(B_Q_TMEM), 0));
-        }
-        if (!bar1_and(q_ok, 256)) failed = true;
 
         float m_run = -INFINITY;  // the row's running max (scaled, log2 units)
         float m_l = -INFINITY;    // reference max of this group's partial sum
@@ -995,7 +1000,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
           float x[128];  // raw scores q.k of the tile's 128 keys
           if (ok) {
             ok = __all_sync(0xffffffffu,
-                            mbar_wait_cluster(bar(B_S_FULL + g), (cnt_ld(3) + (jj >> 1)) & 1));
+                            mbar_wait_cluster(bar(B_S_FULL + g), (cnt_ld(2) + (jj >> 1)) & 1));
             tc_fence_after();
             uint32_t sa[128];  // the whole S row in one request, so the buffer is freed soon
             tmem_ld128(t_lane + kTmemS + g * kBS, sa);
@@ -1016,7 +1021,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
                 if (p.fuse) {
                   const int vb = cnt_ld(0) & 1;
                   ok = ok && __all_sync(0xffffffffu, mbar_wait_cluster(bar(B_TREE + vb),
-                                                                        (cnt_ld(2) >> vb) & 1));
+                                                                        (cnt_ld(1) >> vb) & 1));
                 }
                 const unsigned long long vis0 = row_ok ? lds_u64(vis_row) : 0ull;
                 const unsigned long long vis1 = row_ok ? lds_u64(vis_row + 8) : 0ull;
@@ -1087,7 +1092,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kb = 0; kb < 2; ++kb) {
             if (2 * tile + kb >= u.n_blocks) continue;
-            const int msg_g = cnt_ld(4) + 2 * jj + kb;  // the P block's number in the cluster's stream
+            const int msg_g = cnt_ld(3) + 2 * jj + kb;  // the P block's number in the cluster's stream
             const int ss = msg_g % kStageSlots;
             if (ok && msg_g >= kStageSlots)
               ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar(B_STAGE_FREE + ss),
@@ -1184,11 +1189,10 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) release_unit(i);
         __syncwarp();
         if (lane == 0) {
-          if (ue.builds) cnt_st(2, cnt_ld(2) ^ (1 << (kq & 1)));
+          if (ue.builds) cnt_st(1, cnt_ld(1) ^ (1 << (kq & 1)));
           cnt_st(0, kq + 1);
-          cnt_st(1, cnt_ld(1) + 1);
-          cnt_st(3, cnt_ld(3) + (ue.nt - g + 1) / 2);
-          cnt_st(4, cnt_ld(4) + ue.n_msgs);
+          cnt_st(2, cnt_ld(2) + (ue.nt - g + 1) / 2);
+          cnt_st(3, cnt_ld(3) + ue.n_msgs);
         }
         __syncwarp();
       }
