@@ -927,18 +927,99 @@ __device__ void combine_row(long long row, long long total_rows, int n_split,
   if (lse_out && lane == 0) lse_out[row] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
 }
 
+__device__ void combine_row_wide(long long row, long long total_rows, int n_split,
+                            const __nv_bfloat16* __restrict__ part_o,
+                            const float* __restrict__ part_lse, __nv_bfloat16* __restrict__ out,
+                            float* __restrict__ lse_out) {
+  const int lane = threadIdx.x & 31;
+  // Eight partials at a time: their lse and this lane's 16 dims are all
+  // requested before any is used, so a row of many partials waits for one
+  // memory round trip per eight of them, not two per partial.
+  constexpr int kBatch = 8;
+  float m = -INFINITY;
+  float acc[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+  float wsum = 0.f;
+  for (int s0 = 0; s0 < n_split; s0 += kBatch) {
+    float ls[kBatch];
+    uint4 v[kBatch][2];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int s = s0 + j;
+      if (s < n_split) {
+        ls[j] = part_lse[(long long)s * total_rows + row];
+        const uint4* src =
+            reinterpret_cast<const uint4*>(part_o + ((long long)s * total_rows + row) * kC) +
+            lane * 2;
+        v[j][0] = src[0];
+        v[j][1] = src[1];
+      } else {
+        ls[j] = -INFINITY;
+      }
+    }
+    // the running reference max moves to the batch's max; earlier sums rescale
+    float mb = m;
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) mb = fmaxf(mb, ls[j]);
+    if (mb == -INFINITY) continue;
+    if (mb != m) {
+      const float r = m == -INFINITY ? 0.f : expf(m - mb);
+      wsum *= r;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) acc[k] *= r;
+      m = mb;
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      if (ls[j] == -INFINITY) continue;
+      const float w = expf(ls[j] - m);
+      wsum += w;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const uint32_t wv[4] = {v[j][q].x, v[j][q].y, v[j][q].z, v[j][q].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[e]));
+          acc[8 * q + 2 * e] = fmaf(w, f.x, acc[8 * q + 2 * e]);
+          acc[8 * q + 2 * e + 1] = fmaf(w, f.y, acc[8 * q + 2 * e + 1]);
+        }
+      }
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  uint4* dst = reinterpret_cast<uint4*>(out + row * kC) + lane * 2;
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+    dst[q] = make_uint4(pack_bf16(acc[8 * q + 0] * inv, acc[8 * q + 1] * inv),
+                        pack_bf16(acc[8 * q + 2] * inv, acc[8 * q + 3] * inv),
+                        pack_bf16(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv),
+                        pack_bf16(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv));
+  if (lse_out && lane == 0) lse_out[row] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
+}
+
 // Split-KV merge: one warp per query row. Launched as the programmatic
 // dependent of the step's accept + compaction kernel, it runs beside it and
 // then waits for it before exiting, so work queued after the merge still
 // finds the step complete (without such a predecessor the wait returns at
-// once).
+// once). kWide takes partials eight at a time: faster from five partials up
+// when the rows are few (the q_len 1 steps split over tens of key ranges,
+// where each row's chain of memory round trips is the whole merge); with two
+// partials, or with enough rows for several blocks per SM, the one-at-a-time
+// loop wins, its 48 registers against about 200 keeping more warps resident.
+constexpr int kCombineWideFrom = 5;
+constexpr long long kCombineWideRows = 8LL * 152 * 4;
+template <bool kWide>
 __global__ void __launch_bounds__(256) k_combine(long long total_rows, int n_split,
                                                  const __nv_bfloat16* __restrict__ part_o,
                                                  const float* __restrict__ part_lse,
                                                  __nv_bfloat16* __restrict__ out,
                                                  float* __restrict__ lse_out) {
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (row < total_rows) combine_row(row, total_rows, n_split, part_o, part_lse, out, lse_out);
+  if (row < total_rows) {
+    if (kWide) combine_row_wide(row, total_rows, n_split, part_o, part_lse, out, lse_out);
+    else combine_row(row, total_rows, n_split, part_o, part_lse, out, lse_out);
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
@@ -1154,9 +1235,14 @@ cudaError_t launch_verify_attn_bf16(const ddt_attn_dims& d, const void* q_lat, c
   }
   if (e != cudaSuccess) return e;
   if (pl.n_split == 1) return then != nullptr ? launch_accept_compact(*then, stream) : e;
+  const bool wide = pl.n_split >= kCombineWideFrom && rows <= kCombineWideRows;
   if (then == nullptr) {
-    k_combine<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
-        rows, pl.n_split, part_o, part_lse, static_cast<__nv_bfloat16*>(out), lse);
+    if (wide)
+      k_combine<true><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
+          rows, pl.n_split, part_o, part_lse, static_cast<__nv_bfloat16*>(out), lse);
+    else
+      k_combine<false><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
+          rows, pl.n_split, part_o, part_lse, static_cast<__nv_bfloat16*>(out), lse);
     return cudaGetLastError();
   }
   // accept + compaction first (it needs the tree and the finished cache
@@ -1175,7 +1261,7 @@ cudaError_t launch_verify_attn_bf16(const ddt_attn_dims& d, const void* q_lat, c
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_combine, rows, pl.n_split,
+  return cudaLaunchKernelEx(&cfg, wide ? k_combine<true> : k_combine<false>, rows, pl.n_split,
                             static_cast<const __nv_bfloat16*>(part_o),
                             static_cast<const float*>(part_lse), static_cast<__nv_bfloat16*>(out),
                             lse);
