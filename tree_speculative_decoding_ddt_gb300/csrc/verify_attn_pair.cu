@@ -603,7 +603,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
     if (s_side) {
       // Q of the cluster's first unit depends on no check: it is loaded first.
       // q_lat comes in two halves, one per stage of the key ring, so that each
-      // stage takes its first key tile as soon as its half has moved to TMEM;
+      // stage takes its first key tile as soon as its half is copied to TMEM;
       // q_pe goes to its own area, where it stays as an MMA operand.
       int b0, rt0, sp0;
       unit_coords(p, order, unit_id(cl, G, 0), &b0, &rt0, &sp0);
@@ -654,7 +654,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
       // Per-stage state in bit fields (bit s: stage s), kept in registers:
       // rpar the parity of the key halves loaded into the stage, keyl whether
       // its last user is a key half (else a Q half), qused whether that Q half
-      // was moved to TMEM (by a unit of parity bit s of lqpar; else it was never
+      // was copied to TMEM (by a unit of parity bit s of lqpar; else it was never
       // used); tpar / tused the building units per ancestor-word buffer.
       int kq = 0;  // units with key tiles so far
       int qn = 1;  // Q loads issued (the first unit's at setup)
@@ -688,7 +688,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
           if (i > 0) {
             // the unit's Q goes into both stages once their last user is done:
             // the MMAs of a key half (which also ends the previous unit's reads
-            // of q_pe and of the q_lat in TMEM), a Q half moved to TMEM, or a
+            // of q_pe and of the q_lat in TMEM), a Q half copied to TMEM, or a
             // Q load that was never used
             for (int s = 0; s < 2 && ok; ++s)
               ok = (keyl >> s) & 1 ? mbar_wait_cluster(bar(B_RING_EMPTY + s * kKGroups + kKGroups - 1),
